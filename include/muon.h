@@ -1,0 +1,176 @@
+/*
+ * muon.h - C ABI of the B300 (sm_103a) Muon optimizer step.
+ *
+ * What is computed
+ * ----------------
+ * "How to train a GPT model in 3 minutes: an analysis of modded-nanogpt's
+ * optimizations", section 2 (custom Muon optimizer): Muon replaces AdamW for
+ * the hidden projection matrices. It follows spectral gradient descent, whose
+ * step direction is the orthogonal polar factor U V^T of the update, and it
+ * reaches that factor with a Newton-Schulz iteration instead of an SVD. The
+ * record analysis "2026-05-27_MuddGatedAndDC", section 6.2 (per-parameter
+ * optimizer table), routes projection matrices to Muon and gates to Adam.
+ *
+ * The pages print no formula. This library computes, per matrix, the plainest
+ * reading of that description:
+ *
+ *   1. momentum   buf <- beta*buf + g;  u = g + beta*buf (Nesterov) or u = buf
+ *   2. normalise  X0 = u / (||u||_F + eps)
+ *   3. orient     X = X0^T when rows > cols (n = min(rows,cols) <= m = max)
+ *   4. iterate    A = X X^T;  B = b*A + c*A*A;  X <- a*X + B X      (k times)
+ *   5. restore    O = X^T if step 3 transposed, else X
+ *   6. update     W <- W - lr * s * O,  s = max(1, rows/cols)^0.5 (or 1)
+ *
+ * muon_step runs 1-6, muon_orthogonalize runs 2-5.
+ *
+ * Conventions
+ * -----------
+ * - Every matrix is row-major: element (i, j) sits at ptr + i*ld + j, in
+ *   elements, with ld >= cols. All pointers are DEVICE pointers on the
+ *   handle's device, and the caller owns them.
+ * - Descriptor arrays (muon_matrix*) are HOST arrays. They are read during
+ *   the call and not kept.
+ * - `stream` is a cudaStream_t passed as void*. NULL means the legacy default
+ *   stream. All GPU work is queued on it in order, and no call waits for the
+ *   GPU except muon_get_error and muon_profile_read.
+ * - Arithmetic: operands of the Newton-Schulz products are bf16 and
+ *   accumulation is fp32 on the tensor cores. Momentum, norms and updates use
+ *   fp32 math.
+ * - A call with a matrix set it has not seen before builds a plan: it groups
+ *   the matrices by oriented shape and allocates device workspace
+ *   (cudaMalloc). That first call synchronises the device. Later calls with
+ *   the same shapes reuse the plan and allocate nothing.
+ * - Calls on one handle must not overlap on the GPU, i.e. they must be on
+ *   one stream or otherwise ordered, because they share the plan's workspace.
+ * - Errors: argument errors are found on the host before any launch. They
+ *   return MUON_ERR_INVALID and have no side effect. CUDA errors return
+ *   MUON_ERR_CUDA. A device-side wait that runs past its time limit (about
+ *   two seconds) ends its kernel early and raises a device flag, which
+ *   muon_get_error reports as MUON_ERR_TIMEOUT. muon_last_error gives a
+ *   one-line message for the last failure on the handle.
+ */
+#ifndef MUON_H
+#define MUON_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct muon_ctx* muon_handle;
+
+typedef enum {
+  MUON_OK = 0,
+  MUON_ERR_INVALID = 1,      /* bad argument; nothing was launched */
+  MUON_ERR_CUDA = 2,         /* a CUDA runtime or driver call failed */
+  MUON_ERR_NOMEM = 3,        /* workspace allocation failed */
+  MUON_ERR_UNSUPPORTED = 4,  /* device is not sm_103 / sm_100 class */
+  MUON_ERR_TIMEOUT = 5       /* a device-side bounded wait expired */
+} muon_status;
+
+typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype;
+
+/* One matrix: row-major, device pointer, ld in elements (ld >= cols).
+ * A matrix with rows == 0 or cols == 0 is accepted and skipped. */
+typedef struct {
+  void* ptr;
+  int64_t rows;
+  int64_t cols;
+  int64_t ld;
+  int32_t dtype; /* muon_dtype */
+} muon_matrix;
+
+/* Newton-Schulz and update settings kept by the handle.
+ * steps: iterations k (>= 0). a, b, c: the odd polynomial a*x + b*x^3 + c*x^5
+ * applied to the singular values. eps: added to ||u||_F, outside the square
+ * root. scale_lr_by_shape: nonzero applies s = max(1, rows/cols)^0.5 in step 6,
+ * zero applies s = 1. */
+typedef struct {
+  int32_t steps;
+  float a, b, c;
+  float eps;
+  int32_t scale_lr_by_shape;
+} muon_config;
+
+/* Fills *cfg with the defaults: steps 5, (a,b,c) = (1.5, -0.5, 0), eps 1e-7,
+ * scale_lr_by_shape 1. The cubic coefficients are the iteration's textbook
+ * form; the pages give none. */
+void muon_default_config(muon_config* cfg);
+
+/* Creates a handle on CUDA device `device`. cfg may be NULL (defaults).
+ * Allocates a small device block (error flag). Returns MUON_ERR_UNSUPPORTED
+ * if the device is not compute capability 10.x. *out is NULL on failure. */
+muon_status muon_create(muon_handle* out, int device, const muon_config* cfg);
+
+/* Frees the handle and its workspace after synchronising the device. NULL is
+ * a no-op. */
+muon_status muon_destroy(muon_handle h);
+
+/* Steps 2-5 on `count` matrices: out[j] = NS_k(in[j]), the Newton-Schulz
+ * orthogonalisation of in[j] with `steps` iterations of the polynomial (a, b, c)
+ * and the handle's eps. in[j] and out[j] have the same rows and cols; dtype F32
+ * or BF16 each (all in[] share one dtype, all out[] share one dtype). out[j]
+ * may be in[j] (in place). Distinct out[] must not overlap. count == 0 is a
+ * no-op. */
+muon_status muon_orthogonalize(muon_handle h, const muon_matrix* in, const muon_matrix* out,
+                               int count, int steps, float a, float b, float c, void* stream);
+
+/* Steps 1-6 on `count` matrices with the handle's Newton-Schulz settings:
+ *   momentum[j] <- beta*momentum[j] + grads[j]
+ *   u = grads[j] + beta*momentum[j]   (nesterov != 0)   or   u = momentum[j]
+ *   params[j]  <- params[j] - lr * s_j * NS_k(u)
+ * params: F32 or BF16 (all alike). grads: F32 or BF16 (all alike).
+ * momentum: F32. All three of matrix j have the same rows and cols and must
+ * not overlap one another. count == 0 is a no-op. */
+muon_status muon_step(muon_handle h, const muon_matrix* params, const muon_matrix* grads,
+                      const muon_matrix* momentum, int count, float lr, float beta, int nesterov,
+                      void* stream);
+
+/* Synchronises `stream`, then returns and clears the device error flag
+ * (MUON_OK or MUON_ERR_TIMEOUT), or MUON_ERR_CUDA if the sync failed. */
+muon_status muon_get_error(muon_handle h, void* stream);
+
+/* Static name of a status code. Never NULL. */
+const char* muon_status_string(muon_status s);
+
+/* One-line message for the last failure on h (empty string if none; a fixed
+ * message for h == NULL). Valid until the next call on h. */
+const char* muon_last_error(muon_handle h);
+
+/* Host-only argument checks that muon_orthogonalize / muon_step run before
+ * launching anything. They touch no GPU and can be called without a device.
+ * On failure, msg (if not NULL, capacity msg_len) receives the reason. */
+muon_status muon_check_orthogonalize(const muon_matrix* in, const muon_matrix* out, int count,
+                                     int steps, char* msg, int msg_len);
+muon_status muon_check_step(const muon_matrix* params, const muon_matrix* grads,
+                            const muon_matrix* momentum, int count, char* msg, int msg_len);
+
+/* Host-only plan arithmetic, no GPU: for `count` matrices of shape
+ * rows[j] x cols[j], writes the number of distinct oriented shapes (groups),
+ * the 128x128 upper-triangle tiles of the Gram products X X^T, the 128x256
+ * tiles of the B X products, and the algorithmic flops of one Newton-Schulz
+ * iteration (n(n+1)m for the upper-triangle Gram plus 2 n^2 m for B X, per
+ * matrix, plus n^2(n+1) for A*A when c != 0 is selected by with_c). Any output
+ * pointer may be NULL. */
+muon_status muon_plan_stats(const int64_t* rows, const int64_t* cols, int count, int with_c,
+                            int* groups, int64_t* gram_tiles, int64_t* combine_tiles,
+                            double* flops_per_iter);
+
+/* Kernel timing, for benchmarks. While enabled, each kernel the handle
+ * launches is bracketed by CUDA events on the launching stream.
+ * muon_profile_read synchronises those events, writes per kernel kind the
+ * summed milliseconds and launch counts since the last read (arrays of
+ * MUON_KERNEL_KINDS entries, either may be NULL) and resets the sums. */
+#define MUON_KERNEL_KINDS 8
+/* kernel kinds: 0 momentum+norm, 1 norm, 2 scale+orient, 3 Gram X X^T,
+ * 4 Gram A A (c != 0), 5 combine a X + B X, 6 update, 7 copy out */
+muon_status muon_profile_enable(muon_handle h, int enable);
+muon_status muon_profile_read(muon_handle h, double* ms, int64_t* launches);
+const char* muon_kernel_name(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_H */

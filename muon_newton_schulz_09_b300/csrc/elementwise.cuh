@@ -1,0 +1,361 @@
+// Memory-bound kernels of the Muon step: momentum with the Frobenius norm,
+// scale + cast + orientation of the Newton-Schulz input, and the scaled
+// weight update (or the copy-out of the orthogonalised matrix).
+//
+// The pages fix only that Muon keeps optimizer state ("lower memory than
+// AdamW", "How to train a GPT model in 3 minutes", section 2) and steps the
+// hidden matrices with an orthogonalised update. The momentum form
+// buf <- beta*buf + g with the Nesterov look-ahead u = g + beta*buf, the
+// normalisation X0 = u / (||u||_F + eps), the orientation rule (transpose when
+// rows > cols) and the update W <- W - lr * max(1, rows/cols)^0.5 * O are the
+// stated configuration of this path.
+//
+// All kernels take a table of matrices as a __grid_constant__ parameter and
+// map blocks to matrices by a prefix of per-matrix block counts, so one launch
+// serves a whole batch of mixed shapes. Global accesses are 16-byte vectors
+// whenever alignment allows.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+namespace muon {
+
+constexpr int kEwThreads = 256;
+constexpr int kFlatChunk = 8192;  // elements per block in the flat kernels (4 vectors of 8 per thread)
+constexpr int kTile = 64;         // transpose tile edge
+constexpr int kEwMax = 128;       // matrices per launch
+
+__device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+__device__ __forceinline__ uint16_t f_to_bf16(float x) {
+  __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+template <bool kF32>
+__device__ __forceinline__ void load8(const void* base, int64_t idx, float (&v)[8]) {
+  if (kF32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx);
+    const float4 a = __ldg(p), b = __ldg(p + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + idx));
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      v[2 * h] = __uint_as_float(ww[h] << 16);
+      v[2 * h + 1] = __uint_as_float(ww[h] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <bool kF32>
+__device__ __forceinline__ void store8(void* base, int64_t idx, const float (&v)[8]) {
+  if (kF32) {
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + idx);
+    p[0] = make_float4(v[0], v[1], v[2], v[3]);
+    p[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      w[h] = static_cast<uint32_t>(f_to_bf16(v[2 * h])) | (static_cast<uint32_t>(f_to_bf16(v[2 * h + 1])) << 16);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + idx) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <bool kF32>
+__device__ __forceinline__ float load1(const void* base, int64_t idx) {
+  return kF32 ? static_cast<const float*>(base)[idx] : bf16_to_f(static_cast<const uint16_t*>(base)[idx]);
+}
+
+template <bool kF32>
+__device__ __forceinline__ void store1(void* base, int64_t idx, float v) {
+  if (kF32)
+    static_cast<float*>(base)[idx] = v;
+  else
+    static_cast<uint16_t*>(base)[idx] = f_to_bf16(v);
+}
+
+// Index of the matrix whose block range holds block b (block_begin ascending).
+template <typename Mat>
+__device__ __forceinline__ int owner_of_block(const Mat* m, int count, int b) {
+  int lo = 0, hi = count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (m[mid].block_begin <= b)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ float warp_sum(float s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// K4a: momentum (+ Nesterov) and the per-matrix sum of squares of u.
+// kStep = false skips the momentum and takes u = g: the norm pass of
+// muon_orthogonalize.
+// ---------------------------------------------------------------------------
+
+struct MomMat {
+  const void* g;       // gradient or orthogonalize input (fp32 or bf16)
+  float* buf;          // momentum, fp32
+  uint16_t* u;         // bf16 u, rows x cols contiguous
+  int64_t ld_g, ld_buf;
+  int rows, cols;
+  int vec_ok;          // 16-byte vector path allowed
+  int block_begin;     // first block of this matrix in the launch
+  int nchunks;         // blocks of this matrix = partial sums
+  float* partial;      // nchunks partial sums of u^2
+  int* ticket;         // arrivals; zero between calls (the last block resets it)
+  float* inv;          // out: 1 / (||u||_F + eps)
+};
+
+struct MomArgs {
+  MomMat m[kEwMax];
+  int count;
+  float beta;
+  int nesterov;
+  float eps;
+};
+
+template <bool kStep, bool kSrcF32>
+__global__ void __launch_bounds__(kEwThreads) momentum_norm_kernel(const __grid_constant__ MomArgs a) {
+  const int j = owner_of_block(a.m, a.count, static_cast<int>(blockIdx.x));
+  const MomMat& M = a.m[j];
+  const int chunk = static_cast<int>(blockIdx.x) - M.block_begin;
+  const int64_t cols = M.cols;
+  const int64_t n = static_cast<int64_t>(M.rows) * cols;
+  const int64_t e0 = static_cast<int64_t>(chunk) * kFlatChunk;
+  const int64_t e1 = min(n, e0 + kFlatChunk);
+  const float beta = a.beta;
+  float ss = 0.f;
+
+  if (M.vec_ok) {
+    constexpr int V = kFlatChunk / (kEwThreads * 8);
+    float g[V][8], b[V][8];
+    int64_t gi[V], bi[V], e[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      e[v] = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
+      if (e[v] < e1) {
+        const int64_t row = e[v] / cols, col = e[v] - row * cols;
+        gi[v] = row * M.ld_g + col;
+        bi[v] = row * M.ld_buf + col;
+        load8<kSrcF32>(M.g, gi[v], g[v]);
+        if (kStep) load8<true>(M.buf, bi[v], b[v]);
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      if (e[v] < e1) {
+        float u[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (kStep) {
+            const float nb = beta * b[v][k] + g[v][k];
+            b[v][k] = nb;
+            u[k] = a.nesterov ? g[v][k] + beta * nb : nb;
+          } else {
+            u[k] = g[v][k];
+          }
+          ss += u[k] * u[k];
+        }
+        if (kStep) {
+          store8<true>(M.buf, bi[v], b[v]);
+          store8<false>(M.u, e[v], u);
+        }
+      }
+    }
+  } else {
+    for (int64_t e = e0 + threadIdx.x; e < e1; e += kEwThreads) {
+      const int64_t row = e / cols, col = e - row * cols;
+      const float g = load1<kSrcF32>(M.g, row * M.ld_g + col);
+      float u = g;
+      if (kStep) {
+        const float nb = beta * M.buf[row * M.ld_buf + col] + g;
+        M.buf[row * M.ld_buf + col] = nb;
+        u = a.nesterov ? g + beta * nb : nb;
+        M.u[e] = f_to_bf16(u);
+      }
+      ss += u * u;
+    }
+  }
+
+  // Deterministic norm: every block stores its partial, the last block to
+  // arrive sums the partials in index order.
+  __shared__ float wsum[kEwThreads / 32];
+  __shared__ int is_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ss = warp_sum(ss);
+  if (lane == 0) wsum[warp] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kEwThreads / 32; ++w) s += wsum[w];
+    M.partial[chunk] = s;
+    __threadfence();
+    const int t = atomicAdd(M.ticket, 1);
+    is_last = (t == M.nchunks - 1);
+  }
+  __syncthreads();
+  if (is_last) {
+    __threadfence();
+    float s = 0.f;
+    for (int i = threadIdx.x; i < M.nchunks; i += kEwThreads) s += __ldcg(M.partial + i);
+    s = warp_sum(s);
+    __syncthreads();
+    if (lane == 0) wsum[warp] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kEwThreads / 32; ++w) tot += wsum[w];
+      *M.inv = 1.0f / (sqrtf(tot) + a.eps);
+      *M.ticket = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K1 / K4b / copy-out: dst (optionally transposed) = f(src).
+//   kScale : dst(bf16) = src * inv                  (X0 from u or the input)
+//   kUpdate: dst -= scale * src                     (W <- W - lr*s*O)
+//   kCopy  : dst = src                              (O to the caller's buffer)
+// With transposed != 0 the destination is sc x sr and dst(c, r) = f(src(r, c)),
+// done through a 64 x 64 shared-memory tile so both sides stay coalesced.
+// ---------------------------------------------------------------------------
+
+enum MapMode { kScale = 0, kUpdate = 1, kCopy = 2 };
+
+struct MapMat {
+  const void* src;
+  void* dst;
+  int64_t ld_src, ld_dst;
+  int sr, sc;          // source rows, cols
+  int transposed;
+  int vec_ok;          // both sides allow 16-byte vectors
+  int block_begin;
+  int tiles_c;         // transposed: tiles along the source columns
+  float scale;         // kUpdate: lr * s
+  const float* inv;    // kScale: device scalar
+};
+
+struct MapArgs {
+  MapMat m[kEwMax];
+  int count;
+};
+
+template <int kMode, bool kSrcF32, bool kDstF32>
+__device__ __forceinline__ void map_apply8(const MapMat& M, float f, const float (&s)[8], int64_t di) {
+  float d[8];
+  if (kMode == kUpdate) {
+    load8<kDstF32>(M.dst, di, d);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) d[k] -= f * s[k];
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) d[k] = (kMode == kScale) ? s[k] * f : s[k];
+  }
+  store8<kDstF32>(M.dst, di, d);
+}
+
+template <int kMode, bool kDstF32>
+__device__ __forceinline__ void map_apply1(const MapMat& M, float f, float s, int64_t di) {
+  if (kMode == kUpdate)
+    store1<kDstF32>(M.dst, di, load1<kDstF32>(M.dst, di) - f * s);
+  else
+    store1<kDstF32>(M.dst, di, (kMode == kScale) ? s * f : s);
+}
+
+template <int kMode, bool kSrcF32, bool kDstF32>
+__global__ void __launch_bounds__(kEwThreads) map_kernel(const __grid_constant__ MapArgs a) {
+  const int j = owner_of_block(a.m, a.count, static_cast<int>(blockIdx.x));
+  const MapMat& M = a.m[j];
+  const int blk = static_cast<int>(blockIdx.x) - M.block_begin;
+  const float f = (kMode == kScale) ? __ldg(M.inv) : M.scale;
+
+  if (!M.transposed) {
+    const int64_t cols = M.sc;
+    const int64_t n = static_cast<int64_t>(M.sr) * cols;
+    const int64_t e0 = static_cast<int64_t>(blk) * kFlatChunk;
+    const int64_t e1 = min(n, e0 + kFlatChunk);
+    if (M.vec_ok) {
+      constexpr int V = kFlatChunk / (kEwThreads * 8);
+      float s[V][8];
+      int64_t e[V], di[V];
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        e[v] = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
+        if (e[v] < e1) {
+          const int64_t row = e[v] / cols, col = e[v] - row * cols;
+          di[v] = row * M.ld_dst + col;
+          load8<kSrcF32>(M.src, row * M.ld_src + col, s[v]);
+        }
+      }
+#pragma unroll
+      for (int v = 0; v < V; ++v)
+        if (e[v] < e1) map_apply8<kMode, kSrcF32, kDstF32>(M, f, s[v], di[v]);
+    } else {
+      for (int64_t e = e0 + threadIdx.x; e < e1; e += kEwThreads) {
+        const int64_t row = e / cols, col = e - row * cols;
+        map_apply1<kMode, kDstF32>(M, f, load1<kSrcF32>(M.src, row * M.ld_src + col), row * M.ld_dst + col);
+      }
+    }
+    return;
+  }
+
+  // Transposed: source tile rows r0..r0+63, cols c0..c0+63.
+  __shared__ float tile[kTile][kTile + 1];
+  const int r0 = (blk / M.tiles_c) * kTile;
+  const int c0 = (blk % M.tiles_c) * kTile;
+  const int sub = threadIdx.x >> 3;        // 0..31
+  const int c8 = (threadIdx.x & 7) * 8;    // 0..56
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const int r = p * 32 + sub;
+    const int gr = r0 + r, gc = c0 + c8;
+    float v[8];
+    if (gr < M.sr && gc + 7 < M.sc && M.vec_ok) {
+      load8<kSrcF32>(M.src, static_cast<int64_t>(gr) * M.ld_src + gc, v);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k] = (gr < M.sr && gc + k < M.sc) ? load1<kSrcF32>(M.src, static_cast<int64_t>(gr) * M.ld_src + gc + k)
+                                            : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tile[r][c8 + k] = v[k];
+  }
+  __syncthreads();
+  // Destination rows are source columns c0 + cc, destination columns source rows r0 + rr.
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const int cc = p * 32 + sub;
+    const int dr = c0 + cc, dc = r0 + c8;
+    if (dr >= M.sc) continue;
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = tile[c8 + k][cc];
+    const int64_t di = static_cast<int64_t>(dr) * M.ld_dst + dc;
+    if (dc + 7 < M.sr && M.vec_ok) {
+      map_apply8<kMode, kSrcF32, kDstF32>(M, f, v, di);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (dc + k < M.sr) map_apply1<kMode, kDstF32>(M, f, v[k], di + k);
+    }
+  }
+}
+
+}  // namespace muon

@@ -1,0 +1,1005 @@
+// Host runtime and C ABI of the Muon step (declared in include/muon.h).
+//
+// A call validates its descriptors on the host, finds or builds the plan for
+// its matrix shapes (grouping by oriented shape, workspace, tensor maps, tile
+// lists), then queues the kernels on the caller's stream:
+//
+//   muon_step:          momentum+norm -> scale/orient -> k x (Gram, combine) -> update
+//   muon_orthogonalize: norm          -> scale/orient -> k x (Gram, combine) -> copy out
+//
+// With c != 0 each iteration runs a second Gram pass (A A, with b A added in
+// its epilogue) between the two.
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "../../include/muon.h"
+#include "elementwise.cuh"
+#include "ns_gemm.cuh"
+
+using namespace muon;
+
+namespace {
+
+constexpr int kGramBN = 128, kGramStages = 6;
+constexpr int kCombBN = 256, kCombStages = 4;
+using GramShape = GemmShape<true, kGramBN, kGramStages>;
+using CombShape = GemmShape<false, kCombBN, kCombStages>;
+
+constexpr int64_t kMaxDim = 1 << 20;          // rows or cols
+constexpr int64_t kMaxShort = 32768;          // min(rows, cols): the n x n Gram lives in workspace
+constexpr int64_t kMaxElems = 1ll << 32;      // rows * cols
+constexpr int kMaxSteps = 100000;
+
+const char* kKernelNames[MUON_KERNEL_KINDS] = {"momentum_norm", "norm",          "scale_orient", "gram_xxt",
+                                               "gram_aa",       "combine_ax_bx", "update",       "copy_out"};
+
+enum Kind { K_MOMENTUM = 0, K_NORM = 1, K_SCALE = 2, K_GRAM = 3, K_GRAM_AA = 4, K_COMBINE = 5, K_UPDATE = 6,
+            K_COPY = 7 };
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
+
+size_t elem_size(int32_t dt) { return dt == MUON_F32 ? 4 : 2; }
+
+void put_msg(char* msg, int len, const char* fmt, ...) {
+  if (!msg || len <= 0) return;
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(msg, static_cast<size_t>(len), fmt, ap);
+  va_end(ap);
+}
+
+bool dims_ok(const muon_matrix& m, const char* what, int j, char* msg, int len) {
+  if (m.rows < 0 || m.cols < 0 || m.rows > kMaxDim || m.cols > kMaxDim) {
+    put_msg(msg, len, "%s[%d]: shape %lld x %lld out of range", what, j, (long long)m.rows, (long long)m.cols);
+    return false;
+  }
+  if (m.dtype != MUON_F32 && m.dtype != MUON_BF16) {
+    put_msg(msg, len, "%s[%d]: unknown dtype %d", what, j, (int)m.dtype);
+    return false;
+  }
+  if (m.rows == 0 || m.cols == 0) return true;
+  if (std::min(m.rows, m.cols) > kMaxShort || m.rows * m.cols > kMaxElems) {
+    put_msg(msg, len, "%s[%d]: shape %lld x %lld too large", what, j, (long long)m.rows, (long long)m.cols);
+    return false;
+  }
+  if (m.ld < m.cols) {
+    put_msg(msg, len, "%s[%d]: ld %lld < cols %lld", what, j, (long long)m.ld, (long long)m.cols);
+    return false;
+  }
+  if (m.ptr == nullptr) {
+    put_msg(msg, len, "%s[%d]: null pointer", what, j);
+    return false;
+  }
+  return true;
+}
+
+struct Range {
+  uintptr_t lo, hi;
+  int who;
+};
+
+// Byte range touched by a matrix: [ptr, ptr + ((rows-1)*ld + cols) * size).
+Range range_of(const muon_matrix& m, int who) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(m.ptr);
+  const uintptr_t n = static_cast<uintptr_t>((m.rows - 1) * m.ld + m.cols) * elem_size(m.dtype);
+  return {lo, lo + n, who};
+}
+
+bool any_overlap(std::vector<Range> r, int* a, int* b) {
+  std::sort(r.begin(), r.end(), [](const Range& x, const Range& y) { return x.lo < y.lo; });
+  uintptr_t hi = 0;
+  int hi_who = -1;
+  for (size_t i = 0; i < r.size(); ++i) {
+    if (i > 0 && r[i].lo < hi) {
+      *a = hi_who;
+      *b = r[i].who;
+      return true;
+    }
+    if (r[i].hi > hi) {
+      hi = r[i].hi;
+      hi_who = r[i].who;
+    }
+  }
+  return false;
+}
+
+// ------------------------------------------------------------------ plan
+
+struct MatInfo {
+  int64_t rows = 0, cols = 0;
+  bool skip = false;     // zero-sized
+  bool transposed = false;
+  int group = -1, idx = -1;  // shape group and position within it
+  int64_t n = 0, m = 0;      // oriented shape
+  int64_t nchunks = 0;       // norm partials
+  int64_t partial_off = 0;
+};
+
+struct Group {
+  int64_t n = 0, m = 0;
+  int count = 0;
+  int64_t ld_x = 0, ld_p = 0;
+  size_t x_off[2] = {0, 0}, p_off = 0, a_off = 0;  // byte offsets in the workspace
+};
+
+struct GemmBatch {           // up to kMaxGroups groups served by one launch
+  int first_group = 0, num_groups = 0;
+  int4* gram_tiles = nullptr;
+  int num_gram_tiles = 0;
+  int4* comb_tiles = nullptr;
+  int num_comb_tiles = 0;
+  GemmArgs gram[2];          // X_t -> (b A or A), t parity
+  GemmArgs gram_aa;          // A -> c A A + b A
+  GemmArgs comb[2];          // (B, X_t) -> X_{t+1}
+};
+
+struct Plan {
+  std::vector<std::pair<int64_t, int64_t>> key;
+  std::vector<MatInfo> mats;
+  std::vector<Group> groups;
+  std::vector<GemmBatch> batches;
+  uint8_t* ws = nullptr;
+  size_t ws_bytes = 0;
+  float* partial = nullptr;
+  int* tickets = nullptr;
+  float* inv = nullptr;
+  int4* tiles_dev = nullptr;
+  uint64_t last_use = 0;
+};
+
+}  // namespace
+
+struct muon_ctx {
+  int device = 0;
+  int num_sms = 0;
+  muon_config cfg{};
+  int* err_dev = nullptr;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  std::map<std::vector<std::pair<int64_t, int64_t>>, std::unique_ptr<Plan>> plans;
+  uint64_t use_clock = 0;
+  std::string last_error;
+  // profiling
+  bool profiling = false;
+  struct Rec {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> event_pool;
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+muon_status fail(muon_handle h, muon_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (h) h->last_error = buf;
+  return s;
+}
+
+muon_status cuda_fail(muon_handle h, cudaError_t e, const char* where) {
+  return fail(h, MUON_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+cudaEvent_t pooled_event(muon_handle h) {
+  if (!h->event_pool.empty()) {
+    cudaEvent_t e = h->event_pool.back();
+    h->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct ProfScope {
+  muon_handle h;
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  ProfScope(muon_handle h_, int kind_, cudaStream_t s_) : h(h_), kind(kind_), s(s_) {
+    if (h->profiling) {
+      a = pooled_event(h);
+      cudaEventRecord(a, s);
+    }
+  }
+  ~ProfScope() {
+    if (h->profiling && a) {
+      cudaEvent_t b = pooled_event(h);
+      cudaEventRecord(b, s);
+      h->recs.push_back({kind, a, b});
+    }
+  }
+};
+
+bool encode_map(muon_handle h, CUtensorMap* map, void* base, int64_t inner, int64_t rows, int64_t count,
+                int64_t ld, int box_inner, int box_rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(count)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(rows * ld * 2)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Groups matrices by oriented shape (n <= m), in order of first appearance.
+void group_shapes(const std::vector<std::pair<int64_t, int64_t>>& shapes, std::vector<MatInfo>& mats,
+                  std::vector<Group>& groups) {
+  mats.assign(shapes.size(), MatInfo{});
+  std::map<std::pair<int64_t, int64_t>, int> gid;
+  for (size_t j = 0; j < shapes.size(); ++j) {
+    MatInfo& mi = mats[j];
+    mi.rows = shapes[j].first;
+    mi.cols = shapes[j].second;
+    if (mi.rows == 0 || mi.cols == 0) {
+      mi.skip = true;
+      continue;
+    }
+    mi.transposed = mi.rows > mi.cols;
+    mi.n = std::min(mi.rows, mi.cols);
+    mi.m = std::max(mi.rows, mi.cols);
+    auto it = gid.find({mi.n, mi.m});
+    if (it == gid.end()) {
+      it = gid.emplace(std::make_pair(mi.n, mi.m), static_cast<int>(groups.size())).first;
+      Group g;
+      g.n = mi.n;
+      g.m = mi.m;
+      g.ld_x = round_up(mi.m, 8);
+      g.ld_p = round_up(mi.n, 8);
+      groups.push_back(g);
+    }
+    mi.group = it->second;
+    mi.idx = groups[mi.group].count++;
+    mi.nchunks = ceil_div(mi.rows * mi.cols, kFlatChunk);
+  }
+}
+
+// Tile lists of one batch of groups, sorted by contraction length (longest first).
+void build_tiles(const std::vector<Group>& groups, int g0, int ng, std::vector<int4>& gram,
+                 std::vector<int4>& comb) {
+  struct T {
+    int4 t;
+    int64_t cost;
+  };
+  std::vector<T> gt, ct;
+  for (int gi = 0; gi < ng; ++gi) {
+    const Group& g = groups[g0 + gi];
+    const int nt = static_cast<int>(ceil_div(g.n, 128));
+    const int mt = static_cast<int>(ceil_div(g.m, kCombBN));
+    for (int b = 0; b < g.count; ++b) {
+      for (int I = 0; I < nt; ++I)
+        for (int J = I; J < nt; ++J) gt.push_back({make_int4(gi, b, I, J), ceil_div(g.m, 64)});
+      for (int I = 0; I < nt; ++I)
+        for (int J = 0; J < mt; ++J) ct.push_back({make_int4(gi, b, I, J), ceil_div(g.n, 64)});
+    }
+  }
+  auto by_cost = [](const T& x, const T& y) { return x.cost > y.cost; };
+  std::stable_sort(gt.begin(), gt.end(), by_cost);
+  std::stable_sort(ct.begin(), ct.end(), by_cost);
+  gram.clear();
+  comb.clear();
+  for (auto& x : gt) gram.push_back(x.t);
+  for (auto& x : ct) comb.push_back(x.t);
+}
+
+void free_plan(Plan* p) {
+  if (!p) return;
+  if (p->ws) cudaFree(p->ws);
+  if (p->tiles_dev) cudaFree(p->tiles_dev);
+  p->ws = nullptr;
+  p->tiles_dev = nullptr;
+}
+
+muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t>>& key, Plan** out) {
+  auto plan = std::make_unique<Plan>();
+  Plan& P = *plan;
+  P.key = key;
+  group_shapes(key, P.mats, P.groups);
+
+  // Workspace: per group X ping/pong [count][n][ld_x], B and A [count][n][ld_p];
+  // then per matrix partial sums, tickets and the inverse norm.
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = static_cast<size_t>(round_up(static_cast<int64_t>(off + bytes), 256));
+    return o;
+  };
+  for (Group& g : P.groups) {
+    const size_t xb = static_cast<size_t>(g.count) * g.n * g.ld_x * 2;
+    const size_t pb = static_cast<size_t>(g.count) * g.n * g.ld_p * 2;
+    g.x_off[0] = take(xb);
+    g.x_off[1] = take(xb);
+    g.p_off = take(pb);
+    g.a_off = take(pb);
+  }
+  int64_t nparts = 0;
+  for (MatInfo& mi : P.mats) {
+    mi.partial_off = nparts;
+    nparts += mi.nchunks;
+  }
+  const size_t part_off = take(static_cast<size_t>(std::max<int64_t>(nparts, 1)) * 4);
+  const size_t tick_off = take(P.mats.size() * 4 + 4);
+  const size_t inv_off = take(P.mats.size() * 4 + 4);
+  P.ws_bytes = off;
+
+  cudaError_t e = cudaMalloc(&P.ws, P.ws_bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(h, MUON_ERR_NOMEM, "workspace of %zu bytes: %s", P.ws_bytes, cudaGetErrorString(e));
+  }
+  P.partial = reinterpret_cast<float*>(P.ws + part_off);
+  P.tickets = reinterpret_cast<int*>(P.ws + tick_off);
+  P.inv = reinterpret_cast<float*>(P.ws + inv_off);
+  e = cudaMemset(P.ws, 0, P.ws_bytes);
+  if (e != cudaSuccess) {
+    free_plan(&P);
+    return cuda_fail(h, e, "workspace clear");
+  }
+
+  // GEMM batches and their tile lists.
+  std::vector<int4> all_tiles;
+  std::vector<std::pair<size_t, size_t>> tile_offs;  // per batch: gram offset, comb offset
+  for (int g0 = 0; g0 < static_cast<int>(P.groups.size()); g0 += kMaxGroups) {
+    GemmBatch B;
+    B.first_group = g0;
+    B.num_groups = std::min<int>(kMaxGroups, static_cast<int>(P.groups.size()) - g0);
+    std::vector<int4> gt, ct;
+    build_tiles(P.groups, g0, B.num_groups, gt, ct);
+    B.num_gram_tiles = static_cast<int>(gt.size());
+    B.num_comb_tiles = static_cast<int>(ct.size());
+    tile_offs.push_back({all_tiles.size(), all_tiles.size() + gt.size()});
+    all_tiles.insert(all_tiles.end(), gt.begin(), gt.end());
+    all_tiles.insert(all_tiles.end(), ct.begin(), ct.end());
+    P.batches.push_back(B);
+  }
+  if (!all_tiles.empty()) {
+    e = cudaMalloc(&P.tiles_dev, all_tiles.size() * sizeof(int4));
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      free_plan(&P);
+      return fail(h, MUON_ERR_NOMEM, "tile list: %s", cudaGetErrorString(e));
+    }
+    e = cudaMemcpy(P.tiles_dev, all_tiles.data(), all_tiles.size() * sizeof(int4), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      free_plan(&P);
+      return cuda_fail(h, e, "tile list upload");
+    }
+  }
+
+  for (size_t bi = 0; bi < P.batches.size(); ++bi) {
+    GemmBatch& B = P.batches[bi];
+    B.gram_tiles = P.tiles_dev + tile_offs[bi].first;
+    B.comb_tiles = P.tiles_dev + tile_offs[bi].second;
+    GemmArgs base;
+    memset(&base, 0, sizeof(base));
+    base.num_groups = B.num_groups;
+    base.err = h->err_dev;
+    for (int t = 0; t < 2; ++t) {
+      B.gram[t] = base;
+      B.comb[t] = base;
+      B.gram[t].tiles = B.gram_tiles;
+      B.gram[t].num_tiles = B.num_gram_tiles;
+      B.comb[t].tiles = B.comb_tiles;
+      B.comb[t].num_tiles = B.num_comb_tiles;
+    }
+    B.gram_aa = B.gram[0];
+    for (int gi = 0; gi < B.num_groups; ++gi) {
+      const Group& g = P.groups[B.first_group + gi];
+      uint8_t* xb[2] = {P.ws + g.x_off[0], P.ws + g.x_off[1]};
+      uint16_t* pbuf = reinterpret_cast<uint16_t*>(P.ws + g.p_off);
+      uint16_t* abuf = reinterpret_cast<uint16_t*>(P.ws + g.a_off);
+      bool ok = true;
+      for (int t = 0; t < 2; ++t) {
+        // Gram on X_t: both operands are rows of X_t (K-major), output n x n.
+        ok &= encode_map(h, &B.gram[t].map_a[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 128);
+        B.gram[t].map_b[gi] = B.gram[t].map_a[gi];
+        B.gram[t].grp[gi] = GemmGroup{pbuf, nullptr, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
+                                      static_cast<int>(g.ld_p), static_cast<int>(ceil_div(g.m, 64))};
+        // Combine: A operand = B (n x n, K-major), B operand = X_t MN-major, out = X_{1-t}.
+        ok &= encode_map(h, &B.comb[t].map_a[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 128);
+        ok &= encode_map(h, &B.comb[t].map_b[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 64);
+        B.comb[t].grp[gi] = GemmGroup{reinterpret_cast<uint16_t*>(xb[1 - t]), reinterpret_cast<uint16_t*>(xb[t]),
+                                      g.n * g.ld_x, static_cast<int>(g.n), static_cast<int>(g.m),
+                                      static_cast<int>(g.ld_x), static_cast<int>(ceil_div(g.n, 64))};
+      }
+      // A A pass: operands are rows of A (symmetric), addend A, output B.
+      ok &= encode_map(h, &B.gram_aa.map_a[gi], abuf, g.n, g.n, g.count, g.ld_p, 64, 128);
+      B.gram_aa.map_b[gi] = B.gram_aa.map_a[gi];
+      B.gram_aa.grp[gi] = GemmGroup{pbuf, abuf, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
+                                    static_cast<int>(g.ld_p), static_cast<int>(ceil_div(g.n, 64))};
+      if (!ok) {
+        free_plan(&P);
+        return fail(h, MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed for group %lld x %lld", (long long)g.n,
+                    (long long)g.m);
+      }
+    }
+  }
+  // The clear above ran on the legacy stream; the caller's stream may not be ordered after it.
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    free_plan(&P);
+    return cuda_fail(h, e, "plan synchronize");
+  }
+  *out = plan.get();
+  h->plans[key] = std::move(plan);
+  return MUON_OK;
+}
+
+muon_status get_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t>>& key, Plan** out) {
+  auto it = h->plans.find(key);
+  if (it != h->plans.end()) {
+    it->second->last_use = ++h->use_clock;
+    *out = it->second.get();
+    return MUON_OK;
+  }
+  if (h->plans.size() >= 16) {  // drop the least recently used plan
+    auto victim = h->plans.begin();
+    for (auto i = h->plans.begin(); i != h->plans.end(); ++i)
+      if (i->second->last_use < victim->second->last_use) victim = i;
+    cudaDeviceSynchronize();
+    free_plan(victim->second.get());
+    h->plans.erase(victim);
+  }
+  muon_status s = build_plan(h, key, out);
+  if (s == MUON_OK) (*out)->last_use = ++h->use_clock;
+  return s;
+}
+
+// Plan for the GEMM of a batch: where X_t lives for group gi.
+uint16_t* x_slot(const Plan& P, const MatInfo& mi, int t) {
+  const Group& g = P.groups[mi.group];
+  return reinterpret_cast<uint16_t*>(P.ws + g.x_off[t]) + static_cast<int64_t>(mi.idx) * g.n * g.ld_x;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ launches
+
+muon_status launch_checked(muon_handle h, const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(h, e, what);
+  return MUON_OK;
+}
+
+// Norm pass (kStep = false: u = input) or momentum + norm (kStep = true).
+template <bool kStep>
+muon_status launch_momentum(muon_handle h, const Plan& P, const muon_matrix* src, const muon_matrix* buf, float beta,
+                            int nesterov, cudaStream_t s) {
+  const bool f32 = [&] {
+    for (size_t j = 0; j < P.mats.size(); ++j)
+      if (!P.mats[j].skip) return src[j].dtype == MUON_F32;
+    return false;
+  }();
+  MomArgs a;
+  memset(&a, 0, sizeof(a));
+  a.beta = beta;
+  a.nesterov = nesterov ? 1 : 0;
+  a.eps = h->cfg.eps;
+  int blocks = 0;
+  auto flush = [&]() -> muon_status {
+    if (a.count == 0) return MUON_OK;
+    ProfScope ps(h, kStep ? K_MOMENTUM : K_NORM, s);
+    if (f32)
+      momentum_norm_kernel<kStep, true><<<blocks, kEwThreads, 0, s>>>(a);
+    else
+      momentum_norm_kernel<kStep, false><<<blocks, kEwThreads, 0, s>>>(a);
+    a.count = 0;
+    blocks = 0;
+    return launch_checked(h, "momentum/norm kernel");
+  };
+  for (size_t j = 0; j < P.mats.size(); ++j) {
+    const MatInfo& mi = P.mats[j];
+    if (mi.skip) continue;
+    MomMat& M = a.m[a.count];
+    M.g = src[j].ptr;
+    M.ld_g = src[j].ld;
+    M.buf = kStep ? static_cast<float*>(buf[j].ptr) : nullptr;
+    M.ld_buf = kStep ? buf[j].ld : 0;
+    M.u = kStep ? x_slot(P, mi, 1) : nullptr;  // u lives in the second X buffer until the scale pass reads it
+    M.rows = static_cast<int>(mi.rows);
+    M.cols = static_cast<int>(mi.cols);
+    bool vec = (mi.cols % 8 == 0) && (src[j].ld % 8 == 0) && aligned16(src[j].ptr);
+    if (kStep) vec = vec && (buf[j].ld % 8 == 0) && aligned16(buf[j].ptr);
+    M.vec_ok = vec ? 1 : 0;
+    M.block_begin = blocks;
+    M.nchunks = static_cast<int>(mi.nchunks);
+    M.partial = P.partial + mi.partial_off;
+    M.ticket = P.tickets + j;
+    M.inv = P.inv + j;
+    blocks += M.nchunks;
+    if (++a.count == kEwMax) {
+      muon_status st = flush();
+      if (st != MUON_OK) return st;
+    }
+  }
+  return flush();
+}
+
+// One map launch family: chooses the template by dtypes and mode.
+template <int kMode>
+muon_status launch_map_dispatch(muon_handle h, const MapArgs& a, int blocks, bool src_f32, bool dst_f32,
+                                cudaStream_t s, int kind) {
+  ProfScope ps(h, kind, s);
+  if (src_f32 && dst_f32)
+    map_kernel<kMode, true, true><<<blocks, kEwThreads, 0, s>>>(a);
+  else if (src_f32)
+    map_kernel<kMode, true, false><<<blocks, kEwThreads, 0, s>>>(a);
+  else if (dst_f32)
+    map_kernel<kMode, false, true><<<blocks, kEwThreads, 0, s>>>(a);
+  else
+    map_kernel<kMode, false, false><<<blocks, kEwThreads, 0, s>>>(a);
+  return launch_checked(h, "map kernel");
+}
+
+// kMode = kScale: src = u (step) or input (orthogonalize) in the caller's orientation, dst = X0 slot.
+// kMode = kUpdate / kCopy: src = X_k slot (oriented), dst = params / out in the caller's orientation.
+template <int kMode>
+muon_status launch_map(muon_handle h, const Plan& P, const muon_matrix* user, int xk, float lr, bool scale_mode_user,
+                       cudaStream_t s, int kind) {
+  bool user_f32 = false;
+  for (size_t j = 0; user && j < P.mats.size(); ++j)
+    if (!P.mats[j].skip) {
+      user_f32 = user[j].dtype == MUON_F32;
+      break;
+    }
+  MapArgs a;
+  memset(&a, 0, sizeof(a));
+  int blocks = 0;
+  bool src_f32 = false, dst_f32 = false;
+  auto flush = [&]() -> muon_status {
+    if (a.count == 0) return MUON_OK;
+    muon_status st = launch_map_dispatch<kMode>(h, a, blocks, src_f32, dst_f32, s, kind);
+    a.count = 0;
+    blocks = 0;
+    return st;
+  };
+  for (size_t j = 0; j < P.mats.size(); ++j) {
+    const MatInfo& mi = P.mats[j];
+    if (mi.skip) continue;
+    const Group& g = P.groups[mi.group];
+    MapMat& M = a.m[a.count];
+    M.transposed = mi.transposed ? 1 : 0;
+    if (kMode == kScale) {
+      if (scale_mode_user) {  // orthogonalize: the caller's input
+        M.src = user[j].ptr;
+        M.ld_src = user[j].ld;
+        src_f32 = user_f32;
+      } else {  // step: u, bf16, rows x cols contiguous in the second X buffer
+        M.src = x_slot(P, mi, 1);
+        M.ld_src = mi.cols;
+        src_f32 = false;
+      }
+      M.dst = x_slot(P, mi, 0);
+      M.ld_dst = g.ld_x;
+      M.sr = static_cast<int>(mi.rows);
+      M.sc = static_cast<int>(mi.cols);
+      dst_f32 = false;
+      M.inv = P.inv + j;
+    } else {
+      M.src = x_slot(P, mi, xk);
+      M.ld_src = g.ld_x;
+      M.dst = user[j].ptr;
+      M.ld_dst = user[j].ld;
+      M.sr = static_cast<int>(mi.n);
+      M.sc = static_cast<int>(mi.m);
+      src_f32 = false;
+      dst_f32 = user_f32;
+      const double sc = h->cfg.scale_lr_by_shape ? std::sqrt(std::max(1.0, double(mi.rows) / double(mi.cols))) : 1.0;
+      M.scale = static_cast<float>(double(lr) * sc);
+    }
+    const bool vec = (M.sc % 8 == 0 || M.transposed) && (M.ld_src % 8 == 0) && (M.ld_dst % 8 == 0) &&
+                     aligned16(M.src) && aligned16(M.dst);
+    M.vec_ok = vec ? 1 : 0;
+    M.block_begin = blocks;
+    if (M.transposed) {
+      M.tiles_c = static_cast<int>(ceil_div(M.sc, kTile));
+      blocks += static_cast<int>(ceil_div(M.sr, kTile) * M.tiles_c);
+    } else {
+      M.tiles_c = 0;
+      blocks += static_cast<int>(ceil_div(static_cast<int64_t>(M.sr) * M.sc, kFlatChunk));
+    }
+    if (++a.count == kEwMax) {
+      muon_status st = flush();
+      if (st != MUON_OK) return st;
+    }
+  }
+  return flush();
+}
+
+template <bool kGram, int kBN, int kStages>
+muon_status launch_gemm(muon_handle h, const GemmArgs& a, cudaStream_t s, int kind) {
+  if (a.num_tiles == 0) return MUON_OK;
+  using S = GemmShape<kGram, kBN, kStages>;
+  const int grid = std::min(a.num_tiles, h->num_sms);
+  ProfScope ps(h, kind, s);
+  ns_gemm_kernel<kGram, kBN, kStages><<<grid, kGemmThreads, S::SMEM_BYTES, s>>>(a);
+  return launch_checked(h, "tcgen05 GEMM kernel");
+}
+
+// k Newton-Schulz iterations on X0 (buffer 0). Returns the buffer holding X_k.
+muon_status run_iterations(muon_handle h, const Plan& P, int steps, float a, float b, float c, cudaStream_t s,
+                           int* xk) {
+  int t = 0;
+  for (int it = 0; it < steps; ++it) {
+    for (const GemmBatch& B : P.batches) {
+      muon_status st;
+      if (c == 0.0f) {
+        GemmArgs g = B.gram[t];
+        g.s_acc = b;
+        g.s_e = 0.f;
+        st = launch_gemm<true, kGramBN, kGramStages>(h, g, s, K_GRAM);
+      } else {
+        GemmArgs g = B.gram[t];  // A = X X^T into the A buffer
+        for (int gi = 0; gi < g.num_groups; ++gi) {
+          const Group& grp = P.groups[B.first_group + gi];
+          g.grp[gi].out = reinterpret_cast<uint16_t*>(P.ws + grp.a_off);
+        }
+        g.s_acc = 1.f;
+        g.s_e = 0.f;
+        st = launch_gemm<true, kGramBN, kGramStages>(h, g, s, K_GRAM);
+        if (st != MUON_OK) return st;
+        GemmArgs g2 = B.gram_aa;
+        g2.s_acc = c;
+        g2.s_e = b;
+        st = launch_gemm<true, kGramBN, kGramStages>(h, g2, s, K_GRAM_AA);
+      }
+      if (st != MUON_OK) return st;
+      GemmArgs cb = B.comb[t];
+      cb.s_acc = 1.f;
+      cb.s_e = a;
+      st = launch_gemm<false, kCombBN, kCombStages>(h, cb, s, K_COMBINE);
+      if (st != MUON_OK) return st;
+    }
+    t ^= 1;
+  }
+  *xk = t;
+  return MUON_OK;
+}
+
+std::vector<std::pair<int64_t, int64_t>> shape_key(const muon_matrix* m, int count) {
+  std::vector<std::pair<int64_t, int64_t>> k(static_cast<size_t>(count));
+  for (int j = 0; j < count; ++j) k[j] = {m[j].rows, m[j].cols};
+  return k;
+}
+
+bool all_skipped(const muon_matrix* m, int count) {
+  for (int j = 0; j < count; ++j)
+    if (m[j].rows > 0 && m[j].cols > 0) return false;
+  return true;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+void muon_default_config(muon_config* cfg) {
+  if (!cfg) return;
+  cfg->steps = 5;
+  cfg->a = 1.5f;
+  cfg->b = -0.5f;
+  cfg->c = 0.0f;
+  cfg->eps = 1e-7f;
+  cfg->scale_lr_by_shape = 1;
+}
+
+const char* muon_status_string(muon_status s) {
+  switch (s) {
+    case MUON_OK: return "MUON_OK";
+    case MUON_ERR_INVALID: return "MUON_ERR_INVALID";
+    case MUON_ERR_CUDA: return "MUON_ERR_CUDA";
+    case MUON_ERR_NOMEM: return "MUON_ERR_NOMEM";
+    case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED";
+    case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT";
+  }
+  return "MUON_ERR_UNKNOWN";
+}
+
+const char* muon_kernel_name(int kind) {
+  if (kind < 0 || kind >= MUON_KERNEL_KINDS) return "unknown";
+  return kKernelNames[kind];
+}
+
+const char* muon_last_error(muon_handle h) {
+  if (!h) return "null handle";
+  return h->last_error.c_str();
+}
+
+muon_status muon_check_orthogonalize(const muon_matrix* in, const muon_matrix* out, int count, int steps, char* msg,
+                                     int msg_len) {
+  if (count < 0) {
+    put_msg(msg, msg_len, "count %d < 0", count);
+    return MUON_ERR_INVALID;
+  }
+  if (steps < 0 || steps > kMaxSteps) {
+    put_msg(msg, msg_len, "steps %d out of range", steps);
+    return MUON_ERR_INVALID;
+  }
+  if (count == 0) return MUON_OK;
+  if (!in || !out) {
+    put_msg(msg, msg_len, "null descriptor array");
+    return MUON_ERR_INVALID;
+  }
+  int in_dt = -1, out_dt = -1;
+  std::vector<Range> outs;
+  for (int j = 0; j < count; ++j) {
+    if (!dims_ok(in[j], "in", j, msg, msg_len) || !dims_ok(out[j], "out", j, msg, msg_len)) return MUON_ERR_INVALID;
+    if (in[j].rows != out[j].rows || in[j].cols != out[j].cols) {
+      put_msg(msg, msg_len, "in[%d] and out[%d] differ in shape", j, j);
+      return MUON_ERR_INVALID;
+    }
+    if (in[j].rows == 0 || in[j].cols == 0) continue;
+    if (in_dt < 0) in_dt = in[j].dtype;
+    if (out_dt < 0) out_dt = out[j].dtype;
+    if (in[j].dtype != in_dt || out[j].dtype != out_dt) {
+      put_msg(msg, msg_len, "matrix %d: all inputs must share one dtype and all outputs another", j);
+      return MUON_ERR_INVALID;
+    }
+    outs.push_back(range_of(out[j], j));
+  }
+  int x, y;
+  if (any_overlap(outs, &x, &y)) {
+    put_msg(msg, msg_len, "out[%d] and out[%d] overlap", x, y);
+    return MUON_ERR_INVALID;
+  }
+  return MUON_OK;
+}
+
+muon_status muon_check_step(const muon_matrix* params, const muon_matrix* grads, const muon_matrix* momentum,
+                            int count, char* msg, int msg_len) {
+  if (count < 0) {
+    put_msg(msg, msg_len, "count %d < 0", count);
+    return MUON_ERR_INVALID;
+  }
+  if (count == 0) return MUON_OK;
+  if (!params || !grads || !momentum) {
+    put_msg(msg, msg_len, "null descriptor array");
+    return MUON_ERR_INVALID;
+  }
+  int p_dt = -1, g_dt = -1;
+  std::vector<Range> ranges;
+  for (int j = 0; j < count; ++j) {
+    if (!dims_ok(params[j], "params", j, msg, msg_len) || !dims_ok(grads[j], "grads", j, msg, msg_len) ||
+        !dims_ok(momentum[j], "momentum", j, msg, msg_len))
+      return MUON_ERR_INVALID;
+    if (grads[j].rows != params[j].rows || grads[j].cols != params[j].cols ||
+        momentum[j].rows != params[j].rows || momentum[j].cols != params[j].cols) {
+      put_msg(msg, msg_len, "matrix %d: params, grads and momentum differ in shape", j);
+      return MUON_ERR_INVALID;
+    }
+    if (params[j].rows == 0 || params[j].cols == 0) continue;
+    if (momentum[j].dtype != MUON_F32) {
+      put_msg(msg, msg_len, "momentum[%d]: must be F32", j);
+      return MUON_ERR_INVALID;
+    }
+    if (p_dt < 0) p_dt = params[j].dtype;
+    if (g_dt < 0) g_dt = grads[j].dtype;
+    if (params[j].dtype != p_dt || grads[j].dtype != g_dt) {
+      put_msg(msg, msg_len, "matrix %d: all params must share one dtype and all grads another", j);
+      return MUON_ERR_INVALID;
+    }
+    ranges.push_back(range_of(params[j], j));
+    ranges.push_back(range_of(grads[j], count + j));
+    ranges.push_back(range_of(momentum[j], 2 * count + j));
+  }
+  int x, y;
+  if (any_overlap(ranges, &x, &y)) {
+    const char* names[3] = {"params", "grads", "momentum"};
+    put_msg(msg, msg_len, "%s[%d] and %s[%d] overlap", names[x / count], x % count, names[y / count], y % count);
+    return MUON_ERR_INVALID;
+  }
+  return MUON_OK;
+}
+
+muon_status muon_plan_stats(const int64_t* rows, const int64_t* cols, int count, int with_c, int* groups,
+                            int64_t* gram_tiles, int64_t* combine_tiles, double* flops_per_iter) {
+  if (count < 0 || (count > 0 && (!rows || !cols))) return MUON_ERR_INVALID;
+  std::vector<std::pair<int64_t, int64_t>> key(static_cast<size_t>(count));
+  for (int j = 0; j < count; ++j) {
+    if (rows[j] < 0 || cols[j] < 0) return MUON_ERR_INVALID;
+    key[j] = {rows[j], cols[j]};
+  }
+  std::vector<MatInfo> mats;
+  std::vector<Group> grps;
+  group_shapes(key, mats, grps);
+  int64_t gt = 0, ct = 0;
+  for (const Group& g : grps) {
+    const int64_t nt = ceil_div(g.n, 128);
+    gt += g.count * nt * (nt + 1) / 2;
+    ct += g.count * nt * ceil_div(g.m, kCombBN);
+  }
+  double fl = 0.0;
+  for (const MatInfo& mi : mats) {
+    if (mi.skip) continue;
+    const double n = double(mi.n), m = double(mi.m);
+    fl += n * (n + 1.0) * m + 2.0 * n * n * m;
+    if (with_c) fl += n * n * (n + 1.0);
+  }
+  if (groups) *groups = static_cast<int>(grps.size());
+  if (gram_tiles) *gram_tiles = gt * (with_c ? 2 : 1);
+  if (combine_tiles) *combine_tiles = ct;
+  if (flops_per_iter) *flops_per_iter = fl;
+  return MUON_OK;
+}
+
+muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
+  if (!out) return MUON_ERR_INVALID;
+  *out = nullptr;
+  if (cfg && (cfg->steps < 0 || cfg->steps > kMaxSteps || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->a) ||
+              !std::isfinite(cfg->b) || !std::isfinite(cfg->c)))
+    return MUON_ERR_INVALID;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_ERR_CUDA;
+  }
+  if (device < 0 || device >= ndev) return MUON_ERR_INVALID;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MUON_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return MUON_ERR_UNSUPPORTED;
+  DeviceGuard guard(device);
+  auto h = std::make_unique<muon_ctx>();
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+  muon_default_config(&h->cfg);
+  if (cfg) h->cfg = *cfg;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return MUON_ERR_CUDA;
+  h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  if (cudaMalloc(&h->err_dev, 256) != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_ERR_NOMEM;
+  }
+  if (cudaMemset(h->err_dev, 0, 256) != cudaSuccess) {
+    cudaFree(h->err_dev);
+    return MUON_ERR_CUDA;
+  }
+  cudaError_t e1 = cudaFuncSetAttribute(ns_gemm_kernel<true, kGramBN, kGramStages>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, GramShape::SMEM_BYTES);
+  cudaError_t e2 = cudaFuncSetAttribute(ns_gemm_kernel<false, kCombBN, kCombStages>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, CombShape::SMEM_BYTES);
+  if (e1 != cudaSuccess || e2 != cudaSuccess) {
+    cudaFree(h->err_dev);
+    return MUON_ERR_CUDA;
+  }
+  *out = h.release();
+  return MUON_OK;
+}
+
+muon_status muon_destroy(muon_handle h) {
+  if (!h) return MUON_OK;
+  {
+    DeviceGuard guard(h->device);
+    cudaDeviceSynchronize();
+    for (auto& kv : h->plans) free_plan(kv.second.get());
+    if (h->err_dev) cudaFree(h->err_dev);
+    for (auto& r : h->recs) {
+      cudaEventDestroy(r.a);
+      cudaEventDestroy(r.b);
+    }
+    for (cudaEvent_t e : h->event_pool) cudaEventDestroy(e);
+  }
+  delete h;
+  return MUON_OK;
+}
+
+muon_status muon_orthogonalize(muon_handle h, const muon_matrix* in, const muon_matrix* out, int count, int steps,
+                               float a, float b, float c, void* stream) {
+  if (!h) return MUON_ERR_INVALID;
+  char msg[256] = {0};
+  muon_status st = muon_check_orthogonalize(in, out, count, steps, msg, sizeof(msg));
+  if (st != MUON_OK) return fail(h, st, "%s", msg);
+  if (!std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c))
+    return fail(h, MUON_ERR_INVALID, "non-finite coefficient");
+  if (count == 0 || all_skipped(in, count)) return MUON_OK;
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Plan* P = nullptr;
+  if ((st = get_plan(h, shape_key(in, count), &P)) != MUON_OK) return st;
+  if ((st = launch_momentum<false>(h, *P, in, nullptr, 0.f, 0, s)) != MUON_OK) return st;
+  if ((st = launch_map<kScale>(h, *P, in, 0, 0.f, true, s, K_SCALE)) != MUON_OK) return st;
+  int xk = 0;
+  if ((st = run_iterations(h, *P, steps, a, b, c, s, &xk)) != MUON_OK) return st;
+  return launch_map<kCopy>(h, *P, out, xk, 0.f, false, s, K_COPY);
+}
+
+muon_status muon_step(muon_handle h, const muon_matrix* params, const muon_matrix* grads, const muon_matrix* momentum,
+                      int count, float lr, float beta, int nesterov, void* stream) {
+  if (!h) return MUON_ERR_INVALID;
+  char msg[256] = {0};
+  muon_status st = muon_check_step(params, grads, momentum, count, msg, sizeof(msg));
+  if (st != MUON_OK) return fail(h, st, "%s", msg);
+  if (!std::isfinite(lr) || !std::isfinite(beta)) return fail(h, MUON_ERR_INVALID, "non-finite lr or beta");
+  if (count == 0 || all_skipped(params, count)) return MUON_OK;
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Plan* P = nullptr;
+  if ((st = get_plan(h, shape_key(params, count), &P)) != MUON_OK) return st;
+  if ((st = launch_momentum<true>(h, *P, grads, momentum, beta, nesterov, s)) != MUON_OK) return st;
+  if ((st = launch_map<kScale>(h, *P, nullptr, 0, 0.f, false, s, K_SCALE)) != MUON_OK) return st;
+  int xk = 0;
+  if ((st = run_iterations(h, *P, h->cfg.steps, h->cfg.a, h->cfg.b, h->cfg.c, s, &xk)) != MUON_OK) return st;
+  return launch_map<kUpdate>(h, *P, params, xk, lr, false, s, K_UPDATE);
+}
+
+muon_status muon_get_error(muon_handle h, void* stream) {
+  if (!h) return MUON_ERR_INVALID;
+  DeviceGuard guard(h->device);
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "stream synchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, h->err_dev, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e, "error flag read");
+  if (v != 0) {
+    const int zero = 0;
+    cudaMemcpy(h->err_dev, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    return fail(h, MUON_ERR_TIMEOUT, "a device-side wait expired");
+  }
+  return MUON_OK;
+}
+
+muon_status muon_profile_enable(muon_handle h, int enable) {
+  if (!h) return MUON_ERR_INVALID;
+  h->profiling = enable != 0;
+  return MUON_OK;
+}
+
+muon_status muon_profile_read(muon_handle h, double* ms, int64_t* launches) {
+  if (!h) return MUON_ERR_INVALID;
+  DeviceGuard guard(h->device);
+  double acc[MUON_KERNEL_KINDS] = {0};
+  int64_t cnt[MUON_KERNEL_KINDS] = {0};
+  muon_status st = MUON_OK;
+  for (auto& r : h->recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) st = MUON_ERR_CUDA;
+    float t = 0.f;
+    if (st == MUON_OK && cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) {
+      acc[r.kind] += t;
+      cnt[r.kind] += 1;
+    }
+    h->event_pool.push_back(r.a);
+    h->event_pool.push_back(r.b);
+  }
+  h->recs.clear();
+  for (int k = 0; k < MUON_KERNEL_KINDS; ++k) {
+    if (ms) ms[k] = acc[k];
+    if (launches) launches[k] = cnt[k];
+  }
+  if (st != MUON_OK) cudaGetLastError();
+  return st;
+}
+
+}  // extern "C"

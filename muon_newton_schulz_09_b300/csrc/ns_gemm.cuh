@@ -1,0 +1,336 @@
+// Newton-Schulz products on the 5th-generation tensor cores.
+//
+// One iteration of the Muon orthogonalisation ("How to train a GPT model in
+// 3 minutes", section 2, custom Muon optimizer: a Newton-Schulz iteration in
+// place of an SVD) is X <- a X + (b A + c A A) X with A = X X^T. Two kernels
+// carry it, both instances of the template below:
+//
+//   Gram     (kGram = true):  out = s_acc * (Y Y^T) + s_e * E, Y an n x K
+//            matrix read twice through one K-major tensor map. Only tiles
+//            with tile row <= tile col are computed; the epilogue writes each
+//            off-diagonal tile and its transpose, so the n x n output is full.
+//            With Y = X and s_acc = b it produces B = b A directly (c = 0).
+//            With Y = A (symmetric, so A A = A A^T), s_acc = c, E = A and
+//            s_e = b it produces B = b A + c A A.
+//   Combine  (kGram = false): out = s_acc * (B X) + s_e * E with B K-major
+//            (n x n) and X MN-major (n x m, row-major): E = X, s_e = a gives
+//            X' = a X + B X with the combination done on the fp32
+//            accumulator before the single bf16 rounding.
+//
+// Structure: a persistent grid (one CTA per SM) walks a host-built tile list
+// covering every matrix of every shape group in the batch. Warp 0 issues TMA
+// loads into a ring of shared-memory stages, one thread of warp 1 issues
+// tcgen05.mma into a double-buffered fp32 accumulator in tensor memory, and
+// warps 2-5 drain the accumulator (tcgen05.ld), apply the epilogue and store
+// bf16 to global memory. Every wait is bounded (see mbar_wait_bounded).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace muon {
+
+constexpr int kMaxGroups = 6;   // shape groups served by one launch
+constexpr int kGemmThreads = 192;
+
+struct GemmGroup {
+  uint16_t* out;          // bf16 [count][rows_out][ld_out]
+  const uint16_t* e;      // bf16 addend in the same layout as out, or nullptr
+  int64_t mat_stride;     // elements between consecutive matrices of out and e
+  int rows_out, cols_out, ld_out;
+  int nk;                 // number of 64-wide k-blocks of the contraction
+};
+
+struct GemmArgs {
+  CUtensorMap map_a[kMaxGroups];  // operand A: K-major, box 64 x 128
+  CUtensorMap map_b[kMaxGroups];  // operand B: Gram: same as A; combine: MN-major, box 64 x 64
+  GemmGroup grp[kMaxGroups];
+  const int4* tiles;              // {group, matrix within group, tile row, tile col}
+  int num_tiles;
+  int num_groups;
+  float s_acc;
+  float s_e;
+  int* err;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float x) {
+  __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// v[0..31] += s * e[0..limit), e a bf16 row segment (16-byte aligned when limit >= 32).
+__device__ __forceinline__ void add_row32(float (&v)[32], const uint16_t* e, int limit, float s) {
+  if (limit >= 32) {
+    const uint4* p = reinterpret_cast<const uint4*>(e);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = p[q];
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        v[q * 8 + 2 * h] += s * bf16_bits_to_float(ww[h] & 0xFFFFu);
+        v[q * 8 + 2 * h + 1] += s * bf16_bits_to_float(ww[h] >> 16);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (k < limit) v[k] += s * bf16_bits_to_float(e[k]);
+  }
+}
+
+__device__ __forceinline__ void store_row32(uint16_t* o, const float (&v)[32], int limit) {
+  if (limit >= 32) {
+    uint4* p = reinterpret_cast<uint4*>(o);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      p[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
+                        pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (k < limit) o[k] = to_bf16_bits(v[k]);
+  }
+}
+
+// Waits that must not be cut short by the abort flag: used only to let copies
+// and MMAs already in flight land before the CTA releases its resources.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs / 4) return;
+  }
+}
+
+template <bool kGram, int kBN, int kStages>
+struct GemmShape {
+  static constexpr int BM = 128;
+  static constexpr int BK = 64;
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = kBN * BK * 2;
+  static constexpr uint32_t TMEM_COLS = 2 * kBN;
+  static constexpr uint32_t BAR_BYTES = 8 * (2 * kStages + 5) + 16;
+  // 1024 bytes of slack to align the swizzled tiles to 1024.
+  static constexpr uint32_t SMEM_BYTES = 1024 + kStages * (A_BYTES + B_BYTES) + BAR_BYTES;
+};
+
+template <bool kGram, int kBN, int kStages>
+__global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs args) {
+  using S = GemmShape<kGram, kBN, kStages>;
+  constexpr int BM = S::BM, BK = S::BK;
+  constexpr uint32_t A_BYTES = S::A_BYTES, B_BYTES = S::B_BYTES;
+  constexpr uint32_t kIdesc = instr_desc_bf16(BM, kBN, !kGram);
+  static_assert(kBN == 128 || kBN == 256, "tile width");
+  static_assert(S::TMEM_COLS == 256 || S::TMEM_COLS == 512, "TMEM allocation must be a power of two");
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * B_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(bars);
+  // full[s]: stage s loaded; empty[s]: stage s consumed by the MMAs;
+  // tfull[a]: accumulator a complete; tempty[a]: accumulator a drained; drain: abort path.
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int g = 0; g < args.num_groups; ++g) {
+      tma_prefetch_map(&args.map_a[g]);
+      tma_prefetch_map(&args.map_b[g]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0;        // bit s: stage s has a load in flight or landed
+      uint32_t armed_parity = 0; // bit s: parity of that load's phase
+      for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+        const int4 td = args.tiles[t];
+        const GemmGroup& G = args.grp[td.x];
+        const CUtensorMap* ma = &args.map_a[td.x];
+        const CUtensorMap* mb = &args.map_b[td.x];
+        const bool diag = kGram && (td.z == td.w);
+        const uint32_t bytes = diag ? A_BYTES : A_BYTES + B_BYTES;
+        bool ok = true;
+        for (int kb = 0; kb < G.nk; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), bytes);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          tma_load_3d(smem_u32(sA + stage * A_BYTES), ma, full_bar(stage), kb * BK, td.z * BM, td.y);
+          const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
+          if (kGram) {
+            if (!diag) tma_load_3d(b_dst, mb, full_bar(stage), kb * BK, td.w * kBN, td.y);
+          } else {
+#pragma unroll
+            for (int c = 0; c < kBN / 64; ++c)
+              tma_load_3d(b_dst + c * 8192u, mb, full_bar(stage), td.w * kBN + c * 64, kb * BK, td.y);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) {
+        // Let loads already issued land before the CTA's shared memory is released.
+        for (int s = 0; s < kStages; ++s)
+          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool issued = false;
+      for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+        const int4 td = args.tiles[t];
+        const int nk = args.grp[td.x].nk;
+        const bool diag = kGram && (td.z == td.w);
+        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_addr = diag ? a_addr : smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // K-major: the next 16 k-values are 32 bytes further along each 128-byte row.
+            const uint64_t a_desc = smem_desc_sw128(a_addr + k * 32u, 16u, 1024u);
+            // MN-major: the next 16 k-values are 16 rows (2048 bytes) further down.
+            const uint64_t b_desc = kGram ? smem_desc_sw128(b_addr + k * 32u, 16u, 1024u)
+                                          : smem_desc_sw128(b_addr + k * 2048u, 8192u, 1024u);
+            mma_bf16_ss(d_tmem, a_desc, b_desc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          mma_commit(empty_bar(stage));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (*abort_flag && issued) {
+        mma_commit(drain_bar);
+        mbar_wait_drain(drain_bar, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter .. +31
+    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+      const int4 td = args.tiles[t];
+      const GemmGroup& G = args.grp[td.x];
+      if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
+      tc_fence_after();
+      const int row = td.z * BM + row_in_tile;
+      const bool row_ok = row < G.rows_out;
+      const int64_t ld = G.ld_out;
+      uint16_t* out = G.out + static_cast<int64_t>(td.y) * G.mat_stride;
+      const uint16_t* e = G.e ? G.e + static_cast<int64_t>(td.y) * G.mat_stride : nullptr;
+      const bool mirror = kGram && (td.z != td.w);
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t r[32];
+        tmem_load_32cols(tmem_base + lane_field + static_cast<uint32_t>(acc * kBN + c * 32), r);
+        tmem_load_wait();
+        const int col0 = td.w * kBN + c * 32;
+        const int limit = G.cols_out - col0;
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = args.s_acc * __uint_as_float(r[k]);
+        if (row_ok && limit > 0) {
+          if (e) add_row32(v, e + row * ld + col0, limit, args.s_e);
+          store_row32(out + row * ld + col0, v, limit);
+          if (mirror) {
+            // Transposed copy: for a fixed column the 32 lanes write 32 consecutive elements.
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (k < limit) out[static_cast<int64_t>(col0 + k) * ld + row] = to_bf16_bits(v[k]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
+  }
+}
+
+}  // namespace muon

@@ -1,0 +1,180 @@
+"""CUDA path vs the fp64 oracle on small and ragged cases (GPU).
+
+Every comparison runs the library through its C ABI (via the ctypes binding)
+and the oracle in fp64 on the same bf16- or fp32-valued inputs drawn from
+``workloads.py``. The bar is the relative Frobenius error per matrix, TOL.
+Sizes span several 128-wide tiles and ragged tails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_util import TOL, bf16_ulp, dev, host, rel_f
+
+pytestmark = pytest.mark.gpu
+
+CUBIC = (1.5, -0.5, 0.0)
+QUINTIC = (15 / 8, -10 / 8, 3 / 8)
+
+RAGGED = [(128, 256), (256, 128), (130, 70), (70, 130), (1, 5), (5, 1), (2, 2), (64, 200), (200, 64),
+          (129, 257), (257, 129), (384, 96), (300, 300), (513, 1000)]
+
+
+@pytest.fixture(scope="module")
+def muon():
+    from muon_newton_schulz_09_b300 import Muon
+    with Muon(0) as m:
+        yield m
+
+
+def inputs_for(shapes, dtype="bf16", seed=101, std=1.0):
+    w = wl.small_workload("t", shapes, dtype=dtype, grad_std=std, seed=seed)
+    return w, [wl.gradient(w, j) for j in range(w.count)]
+
+
+def run_orth(muon, xs, in_dtype, out_dtype, steps, coeffs):
+    ins = [dev(x, in_dtype) for x in xs]
+    outs = [torch.empty(x.shape, dtype=torch.float32 if out_dtype == "f32" else torch.bfloat16, device="cuda")
+            for x in xs]
+    muon.orthogonalize(ins, outs, steps=steps, coeffs=coeffs)
+    torch.cuda.synchronize()
+    assert muon.get_error() == 0
+    return [host(o) for o in outs]
+
+
+@pytest.mark.parametrize("in_dtype", ["bf16", "f32"])
+def test_steps0_is_frobenius_normalisation(muon, in_dtype):
+    _, xs = inputs_for(RAGGED, in_dtype, seed=7)
+    got = run_orth(muon, xs, in_dtype, "f32", 0, CUBIC)
+    for x, o in zip(xs, got):
+        want = oracle.frobenius_normalize(x)
+        # X0 is rounded to bf16 once (and u once more for bf16 inputs): 2^-8 relative per element at most.
+        assert rel_f(o, want) < 4e-3, x.shape
+
+
+@pytest.mark.parametrize("coeffs,steps", [(CUBIC, 1), (CUBIC, 5), (QUINTIC, 3)], ids=["cubic1", "cubic5", "quintic3"])
+def test_orthogonalize_ragged_batch(muon, coeffs, steps):
+    _, xs = inputs_for(RAGGED, "bf16", seed=11)
+    got = run_orth(muon, xs, "bf16", "f32", steps, coeffs)
+    for x, o in zip(xs, got):
+        want = oracle.orthogonalize(x, steps, coeffs)
+        assert rel_f(o, want) < TOL, (x.shape, rel_f(o, want))
+
+
+def test_orthogonalize_bf16_out_and_f32_in(muon):
+    _, xs = inputs_for([(256, 640), (640, 256), (100, 100)], "f32", seed=12)
+    got = run_orth(muon, xs, "f32", "bf16", 5, CUBIC)
+    for x, o in zip(xs, got):
+        assert rel_f(o, oracle.orthogonalize(x, 5, CUBIC)) < TOL
+
+
+def test_in_place_and_strided(muon):
+    _, xs = inputs_for([(200, 136), (136, 200)], "bf16", seed=13)
+    wants = [oracle.orthogonalize(x, 5, CUBIC) for x in xs]
+    # in place on padded (ld > cols) views
+    bufs = [torch.zeros(x.shape[0], x.shape[1] + 24, dtype=torch.bfloat16, device="cuda") for x in xs]
+    views = [b[:, :x.shape[1]] for b, x in zip(bufs, xs)]
+    for v, x in zip(views, xs):
+        v.copy_(dev(x))
+    muon.orthogonalize(views, views, steps=5, coeffs=CUBIC)
+    torch.cuda.synchronize()
+    for b, v, w in zip(bufs, views, wants):
+        assert rel_f(host(v), w) < TOL
+        assert torch.count_nonzero(b[:, v.shape[1]:]) == 0  # padding untouched
+
+
+def test_zero_matrix_and_empty(muon):
+    z = torch.zeros(96, 160, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((96, 160), 7.0, device="cuda")
+    empty_in = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
+    empty_out = torch.zeros(0, 64, device="cuda")
+    muon.orthogonalize([z, empty_in], [out, empty_out], steps=5)
+    muon.orthogonalize([], [], steps=5)
+    torch.cuda.synchronize()
+    assert muon.get_error() == 0
+    assert torch.all(out == 0)
+
+
+def test_transpose_equivariance(muon):
+    _, xs = inputs_for([(192, 448)], "bf16", seed=14)
+    x = xs[0]
+    a = run_orth(muon, [x, np.ascontiguousarray(x.T)], "bf16", "f32", 5, CUBIC)
+    assert rel_f(a[1].T, a[0]) < 1e-2
+
+
+def test_deterministic(muon):
+    _, xs = inputs_for([(300, 700), (700, 300), (1024, 1024)], "bf16", seed=15)
+    ins = [dev(x) for x in xs]
+    o1 = [torch.empty(x.shape, device="cuda") for x in xs]
+    o2 = [torch.empty(x.shape, device="cuda") for x in xs]
+    muon.orthogonalize(ins, o1, steps=5)
+    muon.orthogonalize(ins, o2, steps=5)
+    torch.cuda.synchronize()
+    for a, b in zip(o1, o2):
+        assert torch.equal(a, b)
+
+
+# ----------------------------------------------------------------------------- muon_step
+
+def step_case(shapes, grad_dtype, param_dtype, seed, nesterov=True, beta=0.95, zero_momentum=False):
+    w = wl.small_workload("s", shapes, kind="step", dtype=grad_dtype, param_dtype=param_dtype, grad_std=1e-3,
+                          spike_rank=2, spike_gain=20.0, seed=seed, nesterov=nesterov, beta=beta,
+                          zero_momentum=zero_momentum)
+    g = [wl.gradient(w, j) for j in range(w.count)]
+    m = [wl.momentum_buffer(w, j) for j in range(w.count)]
+    p = [wl.parameter(w, j) for j in range(w.count)]
+    return w, g, m, p
+
+
+@pytest.mark.parametrize("nesterov,beta", [(True, 0.95), (False, 0.9), (True, 0.0)])
+def test_step_orthogonal_update_f32_params(muon, nesterov, beta):
+    """f32 params at zero: W' = -lr*s*O exactly enough to read O back, and the momentum in fp32."""
+    shapes = [(256, 768), (768, 256), (130, 70), (384, 384)]
+    w, g, m, _ = step_case(shapes, "bf16", "f32", seed=21, nesterov=nesterov, beta=beta)
+    lr = 0.02
+    P = [torch.zeros(s, device="cuda") for s in shapes]
+    G = [dev(x, "bf16") for x in g]
+    M = [dev(x, "f32") for x in m]
+    muon.step(P, G, M, lr=lr, beta=beta, nesterov=nesterov)
+    torch.cuda.synchronize()
+    assert muon.get_error() == 0
+    for j, (r, c) in enumerate(shapes):
+        w_new, buf_new, o = oracle.muon_step(np.zeros((r, c)), g[j], m[j], lr, beta, nesterov, 5, CUBIC)
+        s = oracle.lr_scale(r, c)
+        assert rel_f(host(M[j]), buf_new) < 1e-6
+        assert rel_f(-host(P[j]) / (lr * s), o) < TOL, (r, c)
+
+
+def test_step_bf16_params(muon):
+    """bf16 params: W' is within one bf16 ulp of the oracle's W', plus 5% of the largest update element."""
+    shapes = [(512, 1536), (1536, 512), (96, 96)]
+    w, g, m, p = step_case(shapes, "bf16", "bf16", seed=22)
+    lr = 0.02
+    P = [dev(x, "bf16") for x in p]
+    G = [dev(x, "bf16") for x in g]
+    M = [dev(x, "f32") for x in m]
+    muon.step(P, G, M, lr=lr, beta=0.95, nesterov=True)
+    torch.cuda.synchronize()
+    for j, (r, c) in enumerate(shapes):
+        w_new, _, o = oracle.muon_step(p[j], g[j], m[j], lr, 0.95, True, 5, CUBIC)
+        upd = lr * oracle.lr_scale(r, c) * np.abs(o).max()
+        err = np.abs(host(P[j]) - w_new)
+        assert np.all(err <= bf16_ulp(w_new) + 0.05 * upd), (r, c, float(err.max()))
+
+
+def test_step_f32_grads_config1(muon):
+    """One fp32 128x256 gradient N(0,1), zero momentum, beta 0.95, 5 cubic iterations."""
+    w = wl.SINGLE_128x256
+    g = wl.gradient(w, 0)
+    m = wl.momentum_buffer(w, 0)
+    P = [torch.zeros(128, 256, device="cuda")]
+    muon.step(P, [dev(g, "f32")], [dev(m, "f32")], lr=1.0, beta=w.beta, nesterov=w.nesterov)
+    torch.cuda.synchronize()
+    _, _, o = oracle.muon_step(np.zeros((128, 256)), g, m, 1.0, w.beta, w.nesterov, 5, CUBIC)
+    got = -host(P[0])
+    assert rel_f(got, o) < TOL
+    # distance to the SVD polar factor is a reported number (about 0.5 after 5 steps), not a pass/fail bound
+    u, _, vt = np.linalg.svd(g.astype(np.float64), full_matrices=False)
+    assert abs(rel_f(got, u @ vt) - rel_f(o, u @ vt)) < 0.02
