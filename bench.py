@@ -1,0 +1,487 @@
+"""Benchmark of the Muon optimizer step on one B300 per rank.
+
+Headline workload: the GPT-2 124M hidden-matrix set, 12 layers x (4x 768x768
+attention q/k/v/o, 768x3072, 3072x768 MLP), bf16 gradients N(0,1e-3) plus a
+rank-4 spike x50, fp32 momentum with beta 0.95 and Nesterov, 5 cubic
+Newton-Schulz iterations, bf16 parameters updated with lr 0.02 * max(1,r/c)^0.5.
+One step = one muon_step call over all 72 matrices.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints one JSON line (rank 0). Under torchrun every rank runs its own replica
+of the workload on its own GPU (weak scaling, no collective on the data path);
+value = all ranks' steps / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "Muon steps/sec at GPT-2 124M hidden-matrix shapes; % BF16 TC peak, HBM GB/s"
+UNIT = "steps/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# DRAM bytes (read + write) per launch of each kernel from one ncu capture, keyed
+# by the hash of the kernel sources they were taken with. A stale hash gives null.
+NCU_TRAFFIC = {
+    "ef55536bd5dbb371": {"combine_ax_bx": 383.2e6},  # ncu --set full, one launch, GPT-2 124M set
+}
+
+KERNEL_SOURCES = ["muon_newton_schulz_09_b300/csrc/ns_gemm.cuh", "muon_newton_schulz_09_b300/csrc/elementwise.cuh",
+                  "muon_newton_schulz_09_b300/csrc/ptx.cuh", "muon_newton_schulz_09_b300/csrc/muon_api.cu"]
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------- distributed host logic
+
+def dist_env() -> tuple:
+    """(rank, local_rank, world_size) from the torchrun environment (defaults for a plain launch)."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def reduce_max(x: float) -> float:
+    """Max of x over ranks (x itself without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def whole_job_rate(steps_per_rank: int, world: int, max_elapsed_s: float) -> float:
+    """Steps per second over the whole job: every rank's steps over the slowest rank's time."""
+    return steps_per_rank * world / max_elapsed_s
+
+
+# ----------------------------------------------------------------------------- work accounting
+
+def workload_of(name: str) -> wl.Workload:
+    return wl.WORKLOADS[name]
+
+
+def oriented(shape) -> tuple:
+    r, c = shape
+    return min(r, c), max(r, c)
+
+
+def kernel_work(w: wl.Workload) -> dict:
+    """Algorithmic work per launch of each kernel kind: ("flops" | "bytes", amount).
+
+    Gram: n(n+1)m flops (upper triangle); combine: 2 n^2 m; A A pass (c != 0):
+    n^2 (n+1). Elementwise kernels: bytes each element must move once
+    (momentum: g + buf read/write + u write; scale: u or input read + X0
+    write; update: O read + W read/write; copy: O read + out write).
+    """
+    gb = 4 if w.dtype == "f32" else 2
+    pb = 4 if w.param_dtype == "f32" else 2
+    elems = w.elements()
+    gram = sum(n * (n + 1) * m for n, m in map(oriented, w.shapes))
+    comb = sum(2 * n * n * m for n, m in map(oriented, w.shapes))
+    aa = sum(n * n * (n + 1) for n, m in map(oriented, w.shapes))
+    work = {"gram_xxt": ("flops", float(gram)), "combine_ax_bx": ("flops", float(comb)),
+            "gram_aa": ("flops", float(aa))}
+    if w.kind == "step":
+        work.update({"momentum_norm": ("bytes", float(elems * (gb + 4 + 4 + 2))),
+                     "scale_orient": ("bytes", float(elems * (2 + 2))),
+                     "update": ("bytes", float(elems * (2 + 2 * pb)))})
+    else:
+        work.update({"norm": ("bytes", float(elems * gb)), "scale_orient": ("bytes", float(elems * (gb + 2))),
+                     "copy_out": ("bytes", float(elems * (2 + 4)))})
+    return work
+
+
+def step_flops(w: wl.Workload) -> float:
+    a, b, c = w.coeffs
+    per = sum(n * (n + 1) * m + 2 * n * n * m + (n * n * (n + 1) if c != 0 else 0) for n, m in map(oriented, w.shapes))
+    return float(per * w.steps)
+
+
+# ----------------------------------------------------------------------------- peaks and clocks
+
+def load_peaks() -> tuple:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.device_index = device_index
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.device_index)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        load = [s for s in sm if mx and s > 0.3 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- oracle timing (host cores)
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_matrix_call(w: wl.Workload, j: int, inputs: dict):
+    import oracle
+    if w.kind == "step":
+        g, m, p = inputs[j]
+        return oracle.muon_step(p, g, m, w.lr, w.beta, w.nesterov, w.steps, w.coeffs, w.eps)
+    (g,) = inputs[j]
+    return oracle.orthogonalize(g, w.steps, w.coeffs, w.eps)
+
+
+def oracle_inputs(w: wl.Workload, j: int) -> tuple:
+    if w.kind == "step":
+        return wl.gradient(w, j), wl.momentum_buffer(w, j), wl.parameter(w, j)
+    return (wl.gradient(w, j),)
+
+
+def matrix_fraction(w: wl.Workload) -> list:
+    """Share of one full step's flops carried by each matrix."""
+    f = [n * (n + 1) * m + 2 * n * n * m for n, m in map(oriented, w.shapes)]
+    tot = float(sum(f))
+    return [x / tot for x in f]
+
+
+def distinct_matrices(w: wl.Workload) -> list:
+    """One matrix index per distinct shape (a layer's worth for the GPT-2 sets)."""
+    seen, out = set(), []
+    for j, s in enumerate(w.shapes):
+        if s not in seen:
+            seen.add(s)
+            out.append(j)
+    return out
+
+
+def time_oracle(w: wl.Workload, budget_s: float, min_calls: int = 1) -> dict:
+    """Runs the oracle on matrices of the workload, cycling over its distinct shapes, for about budget_s.
+
+    Returns the full-workload steps/s extrapolated by each matrix's flop share.
+    """
+    frac = matrix_fraction(w)
+    pick = distinct_matrices(w)
+    inputs = {j: oracle_inputs(w, j) for j in pick}
+    done_frac, elapsed, calls = 0.0, 0.0, 0
+    while calls < min_calls or elapsed < budget_s:
+        j = pick[calls % len(pick)]
+        t0 = time.perf_counter()
+        oracle_matrix_call(w, j, inputs)
+        elapsed += time.perf_counter() - t0
+        done_frac += frac[j]
+        calls += 1
+        if calls >= 10 * len(pick) and elapsed >= 0.5 * budget_s:
+            break
+    return {"value": done_frac / elapsed, "calls": calls, "elapsed_s": elapsed, "fraction": done_frac,
+            "shapes": [list(w.shapes[j]) for j in pick]}
+
+
+# ----------------------------------------------------------------------------- device workload
+
+class DeviceWorkload:
+    """Flat device buffers holding every matrix of the workload (views per matrix)."""
+
+    def __init__(self, w: wl.Workload, device: int):
+        import torch
+        self.w = w
+        td = {"bf16": torch.bfloat16, "f32": torch.float32}
+        n = w.elements()
+        offs = np.cumsum([0] + [r * c for r, c in w.shapes])
+        self.grads_flat = torch.empty(n, dtype=td[w.dtype], device=device)
+        self.grads = [self.grads_flat[offs[j]:offs[j + 1]].view(*w.shapes[j]) for j in range(w.count)]
+        for j in range(w.count):
+            self.grads[j].copy_(torch.from_numpy(wl.gradient(w, j)))
+        if w.kind == "step":
+            self.mom_flat = torch.empty(n, dtype=torch.float32, device=device)
+            self.params_flat = torch.empty(n, dtype=td[w.param_dtype], device=device)
+            self.momentum = [self.mom_flat[offs[j]:offs[j + 1]].view(*w.shapes[j]) for j in range(w.count)]
+            self.params = [self.params_flat[offs[j]:offs[j + 1]].view(*w.shapes[j]) for j in range(w.count)]
+            for j in range(w.count):
+                self.momentum[j].copy_(torch.from_numpy(wl.momentum_buffer(w, j)))
+                self.params[j].copy_(torch.from_numpy(wl.parameter(w, j)))
+        else:
+            self.out_flat = torch.empty(n, dtype=torch.bfloat16, device=device)
+            self.outs = [self.out_flat[offs[j]:offs[j + 1]].view(*w.shapes[j]) for j in range(w.count)]
+
+    def resident_bytes(self) -> int:
+        t = [self.grads_flat] + ([self.mom_flat, self.params_flat] if self.w.kind == "step" else [self.out_flat])
+        return sum(x.numel() * x.element_size() for x in t)
+
+    def run(self, muon, stream=None):
+        w = self.w
+        if w.kind == "step":
+            muon.step(self.params, self.grads, self.momentum, lr=w.lr, beta=w.beta, nesterov=w.nesterov,
+                      stream=stream)
+        else:
+            muon.orthogonalize(self.grads, self.outs, steps=w.steps, coeffs=w.coeffs, stream=stream)
+
+    def result_flat(self):
+        return self.params_flat if self.w.kind == "step" else self.out_flat
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_ours(args) -> dict:
+    import torch
+    import torch.distributed as dist
+    from muon_newton_schulz_09_b300 import Muon
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    w = workload_of(args.workload)
+    dw = DeviceWorkload(w, local_rank)
+    a, b, c = w.coeffs
+    muon = Muon(local_rank, steps=w.steps, a=a, b=b, c=c, eps=w.eps, scale_lr_by_shape=True)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        dw.run(muon)
+    torch.cuda.synchronize()
+    if muon.get_error() != 0:
+        raise RuntimeError("device error flag raised during warm-up")
+
+    # ---- timed region: inputs resident in HBM
+    muon.profile_read()
+    muon.profile(True)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            dw.run(muon)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    muon.profile(False)
+    prof = muon.profile_read()
+    elapsed_s = start.elapsed_time(end) / 1e3
+    if muon.get_error() != 0:
+        raise RuntimeError("device error flag raised during the timed region")
+    max_s = reduce_max(elapsed_s)
+    value = whole_job_rate(args.steps, world, max_s)
+
+    # ---- end to end: H2D of the step's gradients from pinned memory, D2H of the updated parameters
+    h2d_src = dw.grads_flat.cpu().pin_memory()
+    d2h_dst = torch.empty_like(dw.result_flat(), device="cpu").pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        dw.grads_flat.copy_(h2d_src, non_blocking=True)
+        dw.run(muon)
+        d2h_dst.copy_(dw.result_flat(), non_blocking=True)
+    barrier()
+    torch.cuda.synchronize()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(e2e_steps):
+        dw.grads_flat.copy_(h2d_src, non_blocking=True)
+        dw.run(muon)
+        d2h_dst.copy_(dw.result_flat(), non_blocking=True)
+    e2.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_s = reduce_max(s2.elapsed_time(e2) / 1e3)
+    e2e = {"value": whole_job_rate(e2e_steps, world, e2e_s), "unit": UNIT,
+           "h2d_bytes_per_step": h2d_src.numel() * h2d_src.element_size(),
+           "d2h_bytes_per_step": d2h_dst.numel() * d2h_dst.element_size(), "steps": e2e_steps}
+
+    # ---- roofline of the dominant kernel, from the per-kernel events of the timed region
+    peaks, peak_src = load_peaks()
+    sustained = elapsed_s >= 1.0
+    tc_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    work = kernel_work(w)
+    kernels = {}
+    for name, (ms, n) in prof.items():
+        if n == 0:
+            continue
+        kind, amount = work[name]
+        avg_ms = ms / n
+        if kind == "flops":
+            ach = amount / (avg_ms * 1e-3) / 1e12
+            kernels[name] = {"launches": n, "avg_us": avg_ms * 1e3, "share": 0.0, "bound": "tensor",
+                             "achieved": ach, "unit": "TFLOP/s", "frac": ach / tc_peak}
+        else:
+            ach = amount / (avg_ms * 1e-3) / 1e9
+            kernels[name] = {"launches": n, "avg_us": avg_ms * 1e3, "share": 0.0, "bound": "hbm",
+                             "achieved": ach, "unit": "GB/s", "frac": ach / peaks["hbm_gbs"]}
+    total_ms = sum(ms for ms, n in prof.values())
+    for name in kernels:
+        kernels[name]["share"] = prof[name][0] / total_ms
+    top = max(kernels, key=lambda k: prof[k][0])
+    k = kernels[top]
+    traffic = NCU_TRAFFIC.get(source_hash(), {}).get(top)
+    roofline = {"kernel": top, "bound": k["bound"], "achieved": round(k["achieved"], 2),
+                "peak": tc_peak if k["bound"] == "tensor" else peaks["hbm_gbs"], "unit": k["unit"],
+                "frac": round(k["frac"], 4), "traffic": traffic,
+                "peak_source": f"{peak_src} ({'sustained' if sustained and k['bound'] == 'tensor' else 'burst'})"}
+    gpu_launches = int(sum(n for ms, n in prof.values()))
+    gemm_ms = sum(prof[n][0] for n in ("gram_xxt", "gram_aa", "combine_ax_bx"))
+    gemm_tflops = step_flops(w) * args.steps / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generators; random-init weights, no dataset)",
+        "config": {"workload": w.name, "description": w.notes, "matrices": w.count,
+                   "ns_steps": w.steps, "coeffs": list(w.coeffs), "kind": w.kind,
+                   "parallelism": f"replicas x{world} (one full step per GPU, no collective)",
+                   "l2": f"inputs larger than L2: {dw.resident_bytes() / 1e6:.0f} MB resident per step",
+                   "alg_flops_per_step": step_flops(w)},
+        "roofline": roofline,
+        "gemm_tflops_per_step": round(gemm_tflops, 1) if gemm_tflops else None,
+        "kernels": {n: {kk: (round(v, 4) if isinstance(v, float) else v) for kk, v in d.items()}
+                    for n, d in kernels.items()},
+        "e2e": {kk: (round(v, 3) if isinstance(v, float) else v) for kk, v in e2e.items()},
+        "gpu_launches": gpu_launches,
+        "clocks": clk.summary(),
+        "impl": "ours",
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t = time_oracle(w, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(t["value"], 6), "unit": UNIT, "cores": blas_threads(),
+                                "kind": "oracle",
+                                "sample": (f"{t['calls']} single-matrix oracle calls cycling over shapes "
+                                           f"{t['shapes']} ({t['elapsed_s']:.1f} s, {t['fraction']:.3f} of one "
+                                           f"full step by flops), fp64 numpy, extrapolated to the full step")}
+    muon.close()
+    return line
+
+
+def run_reference(args) -> dict:
+    """The oracle (fp64, host cores) as the reference arm: each step is one matrix of the workload."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return {}
+    w = workload_of(args.workload)
+    frac = matrix_fraction(w)
+    pick = distinct_matrices(w)
+    inputs = {j: oracle_inputs(w, j) for j in pick}
+    for i in range(args.warmup):
+        oracle_matrix_call(w, pick[i % len(pick)], inputs)
+    done, t0 = 0.0, time.perf_counter()
+    for i in range(args.steps):
+        j = pick[i % len(pick)]
+        oracle_matrix_call(w, j, inputs)
+        done += frac[j]
+    el = time.perf_counter() - t0
+    value = done / el
+    cores = blas_threads()
+    sample = (f"each step: one matrix of {w.name}, cycling over shapes {[list(w.shapes[j]) for j in pick]}; "
+              f"{done:.3f} of one full step by flops in {el:.1f} s; fp64 numpy")
+    return {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generators)",
+            "config": {"workload": w.name, "description": w.notes, "matrices": w.count, "ns_steps": w.steps,
+                       "coeffs": list(w.coeffs), "kind": w.kind},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.GPT2_124M.name, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line and dist_env()[0] == 0:
+        print(json.dumps(line), flush=True)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,108 @@
+"""The C ABI without a GPU: exports, host-side argument checks and plan arithmetic."""
+import ctypes
+
+import pytest
+
+import muon_newton_schulz_09_b300 as mu
+from muon_newton_schulz_09_b300 import MUON_BF16, MUON_ERR_INVALID, MUON_F32, MUON_OK, MuonMatrix
+
+
+def test_library_exports_every_declared_function():
+    lib = mu.load_library()
+    names = mu.header_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_kernel_names():
+    assert mu.status_string(MUON_OK) == "MUON_OK"
+    assert mu.status_string(5) == "MUON_ERR_TIMEOUT"
+    assert mu.status_string(99) == "MUON_ERR_UNKNOWN"
+    assert [mu.kernel_name(k) for k in range(mu.KERNEL_KINDS)] == [
+        "momentum_norm", "norm", "scale_orient", "gram_xxt", "gram_aa", "combine_ax_bx", "update", "copy_out"]
+
+
+def test_default_config():
+    cfg = mu.MuonConfig()
+    mu.load_library().muon_default_config(ctypes.byref(cfg))
+    assert (cfg.steps, cfg.a, cfg.b, cfg.c, cfg.scale_lr_by_shape) == (5, 1.5, -0.5, 0.0, 1)
+    assert abs(cfg.eps - 1e-7) < 1e-12
+
+
+def test_null_handle_is_invalid():
+    lib = mu.load_library()
+    assert lib.muon_orthogonalize(None, None, None, 0, 5, 1.5, -0.5, 0.0, None) == MUON_ERR_INVALID
+    assert lib.muon_step(None, None, None, None, 0, 0.02, 0.95, 1, None) == MUON_ERR_INVALID
+    assert lib.muon_destroy(None) == MUON_OK
+    assert lib.muon_last_error(None) == b"null handle"
+
+
+def M(ptr, r, c, ld=None, dt=MUON_BF16):
+    return MuonMatrix(ctypes.c_void_p(ptr), r, c, c if ld is None else ld, dt)
+
+
+BASE = 1 << 32
+
+
+def test_check_orthogonalize():
+    ok = [M(BASE, 64, 128)]
+    out = [M(BASE + (1 << 24), 64, 128, dt=MUON_F32)]
+    assert mu.check_orthogonalize(ok, out, 5)[0] == MUON_OK
+    assert mu.check_orthogonalize(ok, ok, 5)[0] == MUON_OK  # in place
+    assert mu.check_orthogonalize([], [], 5)[0] == MUON_OK
+    bad = [
+        ([M(BASE, 64, 128)], [M(BASE + (1 << 24), 64, 127)], 5, "differ in shape"),
+        ([M(BASE, 64, 128, ld=100)], out, 5, "ld"),
+        ([M(0, 64, 128)], out, 5, "null pointer"),
+        ([M(BASE, 64, 128, dt=7)], out, 5, "dtype"),
+        (ok, out, -1, "steps"),
+        ([M(BASE, -1, 128)], [M(BASE, -1, 128)], 5, "out of range"),
+        ([M(BASE, 40000, 40000)], [M(BASE, 40000, 40000)], 5, "too large"),
+        ([M(BASE, 8, 8), M(BASE, 8, 8, dt=MUON_F32)], [M(BASE + 4096, 8, 8), M(BASE + 8192, 8, 8)], 1, "dtype"),
+        ([M(BASE, 8, 8), M(BASE, 8, 8)], [M(BASE + 4096, 8, 8), M(BASE + 4096 + 64, 8, 8)], 1, "overlap"),
+    ]
+    for ins, outs, steps, why in bad:
+        st, msg = mu.check_orthogonalize(ins, outs, steps)
+        assert st == MUON_ERR_INVALID and why in msg, (why, msg)
+
+
+def test_zero_sized_matrices_accepted():
+    assert mu.check_orthogonalize([M(0, 0, 16)], [M(0, 0, 16)], 5)[0] == MUON_OK
+    assert mu.check_step([M(0, 16, 0)], [M(0, 16, 0)], [M(0, 16, 0, dt=MUON_F32)])[0] == MUON_OK
+
+
+def test_check_step():
+    p = [M(BASE, 32, 64)]
+    g = [M(BASE + (1 << 20), 32, 64)]
+    m = [M(BASE + (2 << 20), 32, 64, dt=MUON_F32)]
+    assert mu.check_step(p, g, m)[0] == MUON_OK
+    st, msg = mu.check_step(p, g, [M(BASE + (2 << 20), 32, 64)])
+    assert st == MUON_ERR_INVALID and "F32" in msg
+    st, msg = mu.check_step(p, [M(BASE + 64, 32, 64)], m)
+    assert st == MUON_ERR_INVALID and "overlap" in msg
+    st, msg = mu.check_step(p, [M(BASE + (1 << 20), 32, 65)], m)
+    assert st == MUON_ERR_INVALID and "shape" in msg
+
+
+def test_plan_stats_gpt2_124m():
+    shapes = [(768, 768)] * 4 + [(768, 3072), (3072, 768)]
+    s = mu.plan_stats(shapes * 12)
+    assert s["groups"] == 2
+    # 768 = 6 tiles of 128: 21 upper-triangle Gram tiles per matrix
+    assert s["gram_tiles"] == 72 * 21
+    # combine: 6 row tiles x (3 or 12) column tiles of 256
+    assert s["combine_tiles"] == 48 * 6 * 3 + 24 * 6 * 12
+    n = 768
+    want = 48 * (n * (n + 1) * n + 2 * n * n * n) + 24 * (n * (n + 1) * 3072 + 2 * n * n * 3072)
+    assert s["flops_per_iter"] == pytest.approx(want, rel=1e-12)
+    assert 5 * s["flops_per_iter"] == pytest.approx(9.789e11, rel=1e-3)
+
+
+def test_plan_stats_ragged_and_c():
+    s = mu.plan_stats([(130, 70), (70, 130), (0, 5)], with_c=True)
+    assert s["groups"] == 1
+    assert s["gram_tiles"] == 2 * 2 * 1  # one 1x1 upper triangle per matrix, doubled for the A A pass
+    assert s["combine_tiles"] == 2
+    n, m = 70, 130
+    assert s["flops_per_iter"] == pytest.approx(2 * (n * (n + 1) * m + 2 * n * n * m + n * n * (n + 1)))

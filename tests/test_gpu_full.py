@@ -1,0 +1,90 @@
+"""Full-size workloads on the GPU vs the fp64 oracle, on sampled matrices.
+
+Each test runs the whole workload in one library call, the launch
+configuration the benchmark times, then compares matrices the oracle can
+compute one by one (every Newton-Schulz output depends only on its own
+matrix). The single 4096 x 16384 matrix is compared whole.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+import workloads as wl
+from gpu_util import TOL, bf16_ulp, host, rel_f
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def muon():
+    from muon_newton_schulz_09_b300 import Muon
+    with Muon(0) as m:
+        yield m
+
+
+def _step_check(muon, w, sample):
+    dw = bench.DeviceWorkload(w, 0)
+    p0 = {j: host(dw.params[j]) for j in sample}
+    dw.run(muon)
+    torch.cuda.synchronize()
+    assert muon.get_error() == 0
+    for j in sample:
+        g, m, p = wl.gradient(w, j), wl.momentum_buffer(w, j), wl.parameter(w, j)
+        assert np.array_equal(p0[j], p.astype(np.float64))
+        w_new, buf_new, o = oracle.muon_step(p, g, m, w.lr, w.beta, w.nesterov, w.steps, w.coeffs, w.eps)
+        r, c = w.shapes[j]
+        assert rel_f(host(dw.momentum[j]), buf_new) < 1e-6
+        upd = w.lr * oracle.lr_scale(r, c) * np.abs(o).max()
+        err = np.abs(host(dw.params[j]) - w_new)
+        assert np.all(err <= bf16_ulp(w_new) + 0.05 * upd), (j, float(err.max()))
+    # O itself: the same launch with fp32 parameters at zero, so W' = -lr*s*O
+    dw2 = bench.DeviceWorkload(w, 0)
+    P = [torch.zeros(s, dtype=torch.float32, device="cuda") for s in w.shapes]
+    muon.step(P, dw2.grads, dw2.momentum, lr=w.lr, beta=w.beta, nesterov=w.nesterov)
+    torch.cuda.synchronize()
+    errs = {}
+    for j in sample:
+        r, c = w.shapes[j]
+        _, _, o = oracle.muon_step(np.zeros((r, c)), wl.gradient(w, j), wl.momentum_buffer(w, j), w.lr, w.beta,
+                                   w.nesterov, w.steps, w.coeffs, w.eps)
+        errs[j] = rel_f(-host(P[j]) / (w.lr * oracle.lr_scale(r, c)), o)
+    assert max(errs.values()) < TOL, errs
+    return errs
+
+
+def test_gpt2_124m_full_step(muon):
+    errs = _step_check(muon, wl.GPT2_124M, sample=[0, 3, 4, 5, 40, 70, 71])
+    print("gpt2_124m rel-F per sampled matrix:", errs)
+
+
+def test_gpt2_350m_full_step(muon):
+    errs = _step_check(muon, wl.GPT2_350M, sample=[0, 4, 5, 143])
+    print("gpt2_350m rel-F per sampled matrix:", errs)
+
+
+def test_square_64x1024(muon):
+    w = wl.SQUARE_64x1024
+    dw = bench.DeviceWorkload(w, 0)
+    dw.run(muon)
+    torch.cuda.synchronize()
+    assert muon.get_error() == 0
+    for j in (0, 31, 63):
+        want = oracle.orthogonalize(wl.gradient(w, j), w.steps, w.coeffs, w.eps)
+        assert rel_f(host(dw.outs[j]), want) < TOL
+
+
+@pytest.mark.slow
+def test_illconditioned_4096x16384(muon):
+    w = wl.ILLCOND_4096x16384
+    dw = bench.DeviceWorkload(w, 0)
+    out = torch.empty(w.shapes[0], dtype=torch.float32, device="cuda")
+    muon.orthogonalize(dw.grads, [out], steps=w.steps, coeffs=w.coeffs)
+    torch.cuda.synchronize()
+    assert muon.get_error() == 0
+    g = wl.gradient(w, 0)
+    want = oracle.orthogonalize(g, w.steps, w.coeffs, w.eps)
+    e = rel_f(host(out), want)
+    print("illconditioned rel-F:", e)
+    assert e < TOL
