@@ -169,6 +169,40 @@ muon_status muon_profile_enable(muon_handle h, int enable);
 muon_status muon_profile_read(muon_handle h, double* ms, int64_t* launches);
 const char* muon_kernel_name(int kind);
 
+/* ---------------------------------------------------------------- allocation-free normalisation
+ * The pages have no counterpart to this entry point. It exists for callers
+ * that cannot call cudaMalloc: code whose device memory is owned by another
+ * pool or allocator, plugins whose host framework forbids allocation inside
+ * its callbacks, and loops that must never hit the allocator's implicit
+ * synchronisation. muon_create and the first call of a new shape set
+ * allocate; this function never does.
+ *
+ * For each j: out[j] = in[j] / (||in[j]||_F + eps), the normalisation step
+ * on its own (no Newton-Schulz iteration), with the same kernels as the
+ * other entry points. Shapes, dtypes, layouts and in-place use follow
+ * muon_orthogonalize. It needs no handle and runs on the CURRENT CUDA device,
+ * on which every pointer must live.
+ *
+ * Scratch (partial sums, arrival tickets, inverse norms) lives in a static
+ * device array inside the library, about 33 KB, that every GPU which loads
+ * the library holds until the process exits. Limits: at most
+ * MUON_NOALLOC_MAX_MATRICES matrices per call and at most
+ * MUON_NOALLOC_MAX_ELEMENTS elements in total, counting each matrix in whole
+ * blocks of 8192 elements. A call beyond either limit returns
+ * MUON_ERR_INVALID with the reason in msg, and launches nothing.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress). Make that first call before any stream capture.
+ * All calls share the one array: calls that overlap on the GPU (different
+ * streams without ordering, or several host threads) race and give wrong
+ * results. The tickets are cleared by every call; the other contents are left
+ * over from the last call and are rewritten before use.
+ * msg (capacity msg_len, may be NULL) receives the reason for any failure. */
+#define MUON_NOALLOC_MAX_MATRICES 128
+#define MUON_NOALLOC_MAX_ELEMENTS (1ll << 26)
+muon_status muon_normalize_noalloc(const muon_matrix* in, const muon_matrix* out, int count, float eps,
+                                   void* stream, char* msg, int msg_len);
+
 #ifdef __cplusplus
 }
 #endif

@@ -75,6 +75,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "muon_profile_enable": (c.c_int, [c.c_void_p, c.c_int]),
         "muon_profile_read": (c.c_int, [c.c_void_p, P(c.c_double), P(c.c_int64)]),
         "muon_kernel_name": (c.c_char_p, [c.c_int]),
+        "muon_normalize_noalloc": (c.c_int, [P(MuonMatrix), P(MuonMatrix), c.c_int, c.c_float, c.c_void_p,
+                                             c.c_char_p, c.c_int]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -163,6 +165,23 @@ def _stream_ptr(stream, device) -> ctypes.c_void_p:
     if isinstance(stream, int):
         return ctypes.c_void_p(stream)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def normalize_noalloc(inputs: Sequence, outputs: Sequence, eps: float = 1e-7, stream=None):
+    """out[j] = in[j] / (||in[j]||_F + eps) without any device allocation (muon_normalize_noalloc).
+
+    For callers that cannot allocate device memory. Runs on the current CUDA
+    device; the library keeps its small scratch in a static device array, so
+    calls that overlap on the GPU must not be issued.
+    """
+    import torch
+    lib = load_library()
+    msg = ctypes.create_string_buffer(256)
+    st = lib.muon_normalize_noalloc(matrix_array(inputs), matrix_array(outputs), len(inputs), eps,
+                                    _stream_ptr(stream, torch.cuda.current_device()), msg, 256)
+    if st != MUON_OK:
+        raise MuonError(st, "muon_normalize_noalloc: " + msg.value.decode())
+    return outputs
 
 
 class Muon:
