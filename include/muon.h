@@ -148,14 +148,22 @@ muon_status muon_check_step(const muon_matrix* params, const muon_matrix* grads,
 
 /* Host-only plan arithmetic, no GPU: for `count` matrices of shape
  * rows[j] x cols[j], writes the number of distinct oriented shapes (groups),
- * the 128x128 upper-triangle tiles of the Gram products X X^T, the 128x256
- * tiles of the B X products, and the algorithmic flops of one Newton-Schulz
+ * the 128x256 tiles of the Gram products X X^T that reach the upper triangle,
+ * the 128x256 tiles of the B X products, and the algorithmic flops of one Newton-Schulz
  * iteration (n(n+1)m for the upper-triangle Gram plus 2 n^2 m for B X, per
  * matrix, plus n^2(n+1) for A*A when c != 0 is selected by with_c). Any output
  * pointer may be NULL. */
 muon_status muon_plan_stats(const int64_t* rows, const int64_t* cols, int count, int with_c,
                             int* groups, int64_t* gram_tiles, int64_t* combine_tiles,
                             double* flops_per_iter);
+
+/* Failure-detection self-test. Launches one kernel on `stream` that waits,
+ * through the same bounded wait the GEMM kernels use, on a barrier that
+ * nothing ever arrives at. After limit_ns (1e6 .. 2e9 ns, else
+ * MUON_ERR_INVALID) the wait gives up, the kernel raises the handle's error
+ * flag and returns, so the next muon_get_error reports MUON_ERR_TIMEOUT and
+ * the context stays usable. Nothing traps or faults. */
+muon_status muon_selftest_wait(muon_handle h, int64_t limit_ns, void* stream);
 
 /* Kernel timing, for benchmarks. While enabled, each kernel the handle
  * launches is bracketed by CUDA events on the launching stream.

@@ -75,6 +75,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "muon_profile_enable": (c.c_int, [c.c_void_p, c.c_int]),
         "muon_profile_read": (c.c_int, [c.c_void_p, P(c.c_double), P(c.c_int64)]),
         "muon_kernel_name": (c.c_char_p, [c.c_int]),
+        "muon_selftest_wait": (c.c_int, [c.c_void_p, c.c_int64, c.c_void_p]),
         "muon_normalize_noalloc": (c.c_int, [P(MuonMatrix), P(MuonMatrix), c.c_int, c.c_float, c.c_void_p,
                                              c.c_char_p, c.c_int]),
     }
@@ -218,6 +219,43 @@ class Muon:
         st = self.lib.muon_step(self.handle, matrix_array(params), matrix_array(grads), matrix_array(momentum),
                                 len(params), lr, beta, int(bool(nesterov)), _stream_ptr(stream, self.device))
         self._check(st, "muon_step")
+
+    def prepare_step(self, params: Sequence, grads: Sequence, momentum: Sequence, lr: float, beta: float = 0.95,
+                     nesterov: bool = True, stream=None):
+        """Builds the descriptor arrays once and returns a callable that issues this muon_step.
+
+        For loops that step the same tensors every iteration: the per-call cost is
+        then one ctypes call. The tensors must stay alive and in place.
+        """
+        P, G, M = matrix_array(params), matrix_array(grads), matrix_array(momentum)
+        n, s = len(params), _stream_ptr(stream, self.device)
+        fn, h = self.lib.muon_step, self.handle
+
+        def call():
+            st = fn(h, P, G, M, n, lr, beta, int(bool(nesterov)), s)
+            if st != MUON_OK:
+                self._check(st, "muon_step")
+        return call
+
+    def prepare_orthogonalize(self, inputs: Sequence, outputs: Sequence, steps: Optional[int] = None,
+                              coeffs: Optional[Sequence[float]] = None, stream=None):
+        """Like prepare_step, for muon_orthogonalize."""
+        steps = self.config.steps if steps is None else steps
+        a, b, c = (self.config.a, self.config.b, self.config.c) if coeffs is None else coeffs
+        I, O = matrix_array(inputs), matrix_array(outputs)
+        n, s = len(inputs), _stream_ptr(stream, self.device)
+        fn, h = self.lib.muon_orthogonalize, self.handle
+
+        def call():
+            st = fn(h, I, O, n, int(steps), a, b, c, s)
+            if st != MUON_OK:
+                self._check(st, "muon_orthogonalize")
+        return call
+
+    def selftest_wait(self, limit_ns: int = 50_000_000, stream=None):
+        """Queues the failure-detection self-test (a bounded wait that must expire)."""
+        self._check(self.lib.muon_selftest_wait(self.handle, int(limit_ns), _stream_ptr(stream, self.device)),
+                    "muon_selftest_wait")
 
     def get_error(self, stream=None) -> int:
         return self.lib.muon_get_error(self.handle, _stream_ptr(stream, self.device))

@@ -18,6 +18,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <queue>
 #include <memory>
 #include <string>
 #include <vector>
@@ -30,8 +31,12 @@ using namespace muon;
 
 namespace {
 
-constexpr int kGramBN = 128, kGramStages = 6;
+constexpr int kGramBN = 256, kGramStages = 4;
 constexpr int kCombBN = 256, kCombStages = 4;
+#ifndef MUON_GEMM_CLUSTER
+#define MUON_GEMM_CLUSTER 2
+#endif
+constexpr int kCluster = MUON_GEMM_CLUSTER;  // CTAs sharing one B block through TMA multicast
 using GramShape = GemmShape<true, kGramBN, kGramStages>;
 using CombShape = GemmShape<false, kCombBN, kCombStages>;
 
@@ -136,9 +141,11 @@ struct Group {
 struct GemmBatch {           // up to kMaxGroups groups served by one launch
   int first_group = 0, num_groups = 0;
   int4* gram_tiles = nullptr;
-  int num_gram_tiles = 0;
+  int* gram_begin = nullptr;
+  int num_gram_tiles = 0, gram_grid = 0;
   int4* comb_tiles = nullptr;
-  int num_comb_tiles = 0;
+  int* comb_begin = nullptr;
+  int num_comb_tiles = 0, comb_grid = 0;
   GemmArgs gram[2];          // X_t -> (b A or A), t parity
   GemmArgs gram_aa;          // A -> c A A + b A
   GemmArgs comb[2];          // (B, X_t) -> X_{t+1}
@@ -155,6 +162,7 @@ struct Plan {
   int* tickets = nullptr;
   float* inv = nullptr;
   int4* tiles_dev = nullptr;
+  int* begin_dev = nullptr;
   uint64_t last_use = 0;
 };
 
@@ -163,6 +171,7 @@ struct Plan {
 struct muon_ctx {
   int device = 0;
   int num_sms = 0;
+  int max_lists = 0;  // GEMM tile lists run at once: co-resident clusters (or CTAs)
   muon_config cfg{};
   int* err_dev = nullptr;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -283,40 +292,70 @@ void group_shapes(const std::vector<std::pair<int64_t, int64_t>>& shapes, std::v
   }
 }
 
-// Tile lists of one batch of groups, sorted by contraction length (longest first).
-void build_tiles(const std::vector<Group>& groups, int g0, int ng, std::vector<int4>& gram,
-                 std::vector<int4>& comb) {
-  struct T {
-    int4 t;
-    int64_t cost;
-  };
-  std::vector<T> gt, ct;
+// One GEMM launch's schedule: tiles grouped by CTA, and CTA b's range
+// [begin[b], begin[b+1]) in `tiles`.
+struct Schedule {
+  std::vector<int4> tiles;
+  std::vector<int> begin;
+};
+
+// Longest-processing-time-first assignment: tiles sorted by contraction
+// length, each given to the CTA with the least work so far. Every CTA's list
+// stays in decreasing-cost order.
+Schedule lpt_schedule(std::vector<std::pair<int4, int64_t>> work, int max_lists) {
+  std::stable_sort(work.begin(), work.end(),
+                   [](const std::pair<int4, int64_t>& x, const std::pair<int4, int64_t>& y) { return x.second > y.second; });
+  Schedule sc;
+  const int ctas = static_cast<int>(std::min<size_t>(work.size(), static_cast<size_t>(std::max(1, max_lists))));
+  std::vector<std::vector<int4>> per(ctas);
+  using Load = std::pair<int64_t, int>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int b = 0; b < ctas; ++b) heap.push({0, b});
+  for (const auto& w : work) {
+    Load l = heap.top();
+    heap.pop();
+    per[l.second].push_back(w.first);
+    heap.push({l.first + w.second, l.second});
+  }
+  sc.begin.push_back(0);
+  for (int b = 0; b < ctas; ++b) {
+    sc.tiles.insert(sc.tiles.end(), per[b].begin(), per[b].end());
+    sc.begin.push_back(static_cast<int>(sc.tiles.size()));
+  }
+  return sc;
+}
+
+// Gram and combine schedules of one batch of groups. A tile's cost is its
+// number of k-blocks times its width in 128-column units. Gram tiles are
+// 128 x 256 and cover the upper triangle: tile row I <= 2J + 1 in tile column J.
+void build_tiles(const std::vector<Group>& groups, int g0, int ng, int max_lists, Schedule& gram, Schedule& comb) {
+  std::vector<std::pair<int4, int64_t>> gt, ct;
   for (int gi = 0; gi < ng; ++gi) {
     const Group& g = groups[g0 + gi];
     const int nt = static_cast<int>(ceil_div(g.n, 128));
+    const int gt2 = static_cast<int>(ceil_div(g.n, kGramBN));
     const int mt = static_cast<int>(ceil_div(g.m, kCombBN));
+    // With clusters, an entry is the first tile row of a group of kCluster consecutive rows.
     for (int b = 0; b < g.count; ++b) {
-      for (int I = 0; I < nt; ++I)
-        for (int J = I; J < nt; ++J) gt.push_back({make_int4(gi, b, I, J), ceil_div(g.m, 64)});
-      for (int I = 0; I < nt; ++I)
-        for (int J = 0; J < mt; ++J) ct.push_back({make_int4(gi, b, I, J), ceil_div(g.n, 64)});
+      for (int J = 0; J < gt2; ++J)
+        for (int I = 0; I < std::min(2 * J + 2, nt); I += kCluster)
+          gt.push_back({make_int4(gi, b, I, J), 2 * ceil_div(g.m, 64)});
+      for (int I = 0; I < nt; I += kCluster)
+        for (int J = 0; J < mt; ++J) ct.push_back({make_int4(gi, b, I, J), 2 * ceil_div(g.n, 64)});
     }
   }
-  auto by_cost = [](const T& x, const T& y) { return x.cost > y.cost; };
-  std::stable_sort(gt.begin(), gt.end(), by_cost);
-  std::stable_sort(ct.begin(), ct.end(), by_cost);
-  gram.clear();
-  comb.clear();
-  for (auto& x : gt) gram.push_back(x.t);
-  for (auto& x : ct) comb.push_back(x.t);
+  gram = lpt_schedule(std::move(gt), max_lists);
+  comb = lpt_schedule(std::move(ct), max_lists);
 }
 
 void free_plan(Plan* p) {
   if (!p) return;
   if (p->ws) cudaFree(p->ws);
   if (p->tiles_dev) cudaFree(p->tiles_dev);
+  if (p->begin_dev) cudaFree(p->begin_dev);
   p->ws = nullptr;
   p->tiles_dev = nullptr;
+  p->begin_dev = nullptr;
 }
 
 muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t>>& key, Plan** out) {
@@ -365,40 +404,56 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
     return cuda_fail(h, e, "workspace clear");
   }
 
-  // GEMM batches and their tile lists.
+  // GEMM batches and their schedules.
   std::vector<int4> all_tiles;
-  std::vector<std::pair<size_t, size_t>> tile_offs;  // per batch: gram offset, comb offset
+  std::vector<int> all_begin;
+  struct Offs {
+    size_t gt, gb, ct, cb;
+  };
+  std::vector<Offs> offs;
   for (int g0 = 0; g0 < static_cast<int>(P.groups.size()); g0 += kMaxGroups) {
     GemmBatch B;
     B.first_group = g0;
     B.num_groups = std::min<int>(kMaxGroups, static_cast<int>(P.groups.size()) - g0);
-    std::vector<int4> gt, ct;
-    build_tiles(P.groups, g0, B.num_groups, gt, ct);
-    B.num_gram_tiles = static_cast<int>(gt.size());
-    B.num_comb_tiles = static_cast<int>(ct.size());
-    tile_offs.push_back({all_tiles.size(), all_tiles.size() + gt.size()});
-    all_tiles.insert(all_tiles.end(), gt.begin(), gt.end());
-    all_tiles.insert(all_tiles.end(), ct.begin(), ct.end());
+    Schedule gs, cs;
+    build_tiles(P.groups, g0, B.num_groups, h->max_lists, gs, cs);
+    B.num_gram_tiles = static_cast<int>(gs.tiles.size());
+    B.gram_grid = static_cast<int>(gs.begin.size()) - 1;
+    B.num_comb_tiles = static_cast<int>(cs.tiles.size());
+    B.comb_grid = static_cast<int>(cs.begin.size()) - 1;
+    Offs o{all_tiles.size(), all_begin.size(), 0, 0};
+    all_tiles.insert(all_tiles.end(), gs.tiles.begin(), gs.tiles.end());
+    all_begin.insert(all_begin.end(), gs.begin.begin(), gs.begin.end());
+    o.ct = all_tiles.size();
+    o.cb = all_begin.size();
+    all_tiles.insert(all_tiles.end(), cs.tiles.begin(), cs.tiles.end());
+    all_begin.insert(all_begin.end(), cs.begin.begin(), cs.begin.end());
+    offs.push_back(o);
     P.batches.push_back(B);
   }
   if (!all_tiles.empty()) {
     e = cudaMalloc(&P.tiles_dev, all_tiles.size() * sizeof(int4));
-    if (e != cudaSuccess) {
+    cudaError_t e2 = cudaMalloc(&P.begin_dev, all_begin.size() * sizeof(int));
+    if (e != cudaSuccess || e2 != cudaSuccess) {
       cudaGetLastError();
       free_plan(&P);
-      return fail(h, MUON_ERR_NOMEM, "tile list: %s", cudaGetErrorString(e));
+      return fail(h, MUON_ERR_NOMEM, "tile schedule: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
     }
     e = cudaMemcpy(P.tiles_dev, all_tiles.data(), all_tiles.size() * sizeof(int4), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(P.begin_dev, all_begin.data(), all_begin.size() * sizeof(int), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
       free_plan(&P);
-      return cuda_fail(h, e, "tile list upload");
+      return cuda_fail(h, e, "tile schedule upload");
     }
   }
 
   for (size_t bi = 0; bi < P.batches.size(); ++bi) {
     GemmBatch& B = P.batches[bi];
-    B.gram_tiles = P.tiles_dev + tile_offs[bi].first;
-    B.comb_tiles = P.tiles_dev + tile_offs[bi].second;
+    B.gram_tiles = P.tiles_dev + offs[bi].gt;
+    B.gram_begin = P.begin_dev + offs[bi].gb;
+    B.comb_tiles = P.tiles_dev + offs[bi].ct;
+    B.comb_begin = P.begin_dev + offs[bi].cb;
     GemmArgs base;
     memset(&base, 0, sizeof(base));
     base.num_groups = B.num_groups;
@@ -407,9 +462,13 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
       B.gram[t] = base;
       B.comb[t] = base;
       B.gram[t].tiles = B.gram_tiles;
+      B.gram[t].cta_begin = B.gram_begin;
       B.gram[t].num_tiles = B.num_gram_tiles;
+      B.gram[t].grid = B.gram_grid;
       B.comb[t].tiles = B.comb_tiles;
+      B.comb[t].cta_begin = B.comb_begin;
       B.comb[t].num_tiles = B.num_comb_tiles;
+      B.comb[t].grid = B.comb_grid;
     }
     B.gram_aa = B.gram[0];
     for (int gi = 0; gi < B.num_groups; ++gi) {
@@ -636,12 +695,32 @@ muon_status launch_map(muon_handle h, const Plan& P, const muon_matrix* user, in
 }
 
 template <bool kGram, int kBN, int kStages>
+cudaLaunchConfig_t gemm_config(int lists, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(lists * kCluster), 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = GemmShape<kGram, kBN, kStages>::SMEM_BYTES;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <bool kGram, int kBN, int kStages>
 muon_status launch_gemm(muon_handle h, const GemmArgs& a, cudaStream_t s, int kind) {
   if (a.num_tiles == 0) return MUON_OK;
-  using S = GemmShape<kGram, kBN, kStages>;
-  const int grid = std::min(a.num_tiles, h->num_sms);
   ProfScope ps(h, kind, s);
-  ns_gemm_kernel<kGram, kBN, kStages><<<grid, kGemmThreads, S::SMEM_BYTES, s>>>(a);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = gemm_config<kGram, kBN, kStages>(a.grid, s, attr);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kCluster>, a);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(h, e, "tcgen05 GEMM launch");
+  }
   return launch_checked(h, "tcgen05 GEMM kernel");
 }
 
@@ -683,6 +762,21 @@ muon_status run_iterations(muon_handle h, const Plan& P, int steps, float a, flo
   }
   *xk = t;
   return MUON_OK;
+}
+
+// Failure-detection self-test: one thread waits, through the GEMMs' bounded
+// wait, on a barrier that nothing arrives at.
+__global__ void wait_selftest_kernel(int* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+  __syncthreads();
 }
 
 std::vector<std::pair<int64_t, int64_t>> shape_key(const muon_matrix* m, int count) {
@@ -835,7 +929,7 @@ muon_status muon_plan_stats(const int64_t* rows, const int64_t* cols, int count,
   int64_t gt = 0, ct = 0;
   for (const Group& g : grps) {
     const int64_t nt = ceil_div(g.n, 128);
-    gt += g.count * nt * (nt + 1) / 2;
+    for (int64_t J = 0; J < ceil_div(g.n, kGramBN); ++J) gt += g.count * std::min<int64_t>(2 * J + 2, nt);
     ct += g.count * nt * ceil_div(g.m, kCombBN);
   }
   double fl = 0.0;
@@ -887,13 +981,29 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
     cudaFree(h->err_dev);
     return MUON_ERR_CUDA;
   }
-  cudaError_t e1 = cudaFuncSetAttribute(ns_gemm_kernel<true, kGramBN, kGramStages>,
+  cudaError_t e1 = cudaFuncSetAttribute(ns_gemm_kernel<true, kGramBN, kGramStages, kCluster>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, GramShape::SMEM_BYTES);
-  cudaError_t e2 = cudaFuncSetAttribute(ns_gemm_kernel<false, kCombBN, kCombStages>,
+  cudaError_t e2 = cudaFuncSetAttribute(ns_gemm_kernel<false, kCombBN, kCombStages, kCluster>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, CombShape::SMEM_BYTES);
   if (e1 != cudaSuccess || e2 != cudaSuccess) {
     cudaFree(h->err_dev);
     return MUON_ERR_CUDA;
+  }
+  // Persistent grids: as many tile lists as clusters (or CTAs) that can be resident at once.
+  h->max_lists = h->num_sms / kCluster;
+  if (kCluster > 1) {
+    cudaLaunchAttribute attr[1];
+    int n1 = 0, n2 = 0;
+    cudaLaunchConfig_t c1 = gemm_config<true, kGramBN, kGramStages>(1, nullptr, attr);
+    e1 = cudaOccupancyMaxActiveClusters(&n1, ns_gemm_kernel<true, kGramBN, kGramStages, kCluster>, &c1);
+    cudaLaunchConfig_t c2 = gemm_config<false, kCombBN, kCombStages>(1, nullptr, attr);
+    e2 = cudaOccupancyMaxActiveClusters(&n2, ns_gemm_kernel<false, kCombBN, kCombStages, kCluster>, &c2);
+    if (e1 != cudaSuccess || e2 != cudaSuccess || n1 < 1 || n2 < 1) {
+      cudaGetLastError();
+      cudaFree(h->err_dev);
+      return MUON_ERR_UNSUPPORTED;
+    }
+    h->max_lists = std::min(n1, n2);
   }
   *out = h.release();
   return MUON_OK;
@@ -969,6 +1079,14 @@ muon_status muon_get_error(muon_handle h, void* stream) {
     return fail(h, MUON_ERR_TIMEOUT, "a device-side wait expired");
   }
   return MUON_OK;
+}
+
+muon_status muon_selftest_wait(muon_handle h, int64_t limit_ns, void* stream) {
+  if (!h) return MUON_ERR_INVALID;
+  if (limit_ns < 1000000 || limit_ns > 2000000000) return fail(h, MUON_ERR_INVALID, "limit_ns out of [1e6, 2e9]");
+  DeviceGuard guard(h->device);
+  wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(h->err_dev, static_cast<uint64_t>(limit_ns));
+  return launch_checked(h, "wait self-test kernel");
 }
 
 muon_status muon_profile_enable(muon_handle h, int enable) {

@@ -6,9 +6,11 @@
 // carry it, both instances of the template below:
 //
 //   Gram     (kGram = true):  out = s_acc * (Y Y^T) + s_e * E, Y an n x K
-//            matrix read twice through one K-major tensor map. Only tiles
-//            with tile row <= tile col are computed; the epilogue writes each
-//            off-diagonal tile and its transpose, so the n x n output is full.
+//            matrix read through one K-major tensor map. Tiles are 128 rows x
+//            256 columns; only tiles that reach the upper triangle are
+//            computed (tile row I <= 2J + 1 for tile column J), and the
+//            epilogue writes each 128 x 128 block above the diagonal in place
+//            and transposed, so the n x n output is full.
 //            With Y = X and s_acc = b it produces B = b A directly (c = 0).
 //            With Y = A (symmetric, so A A = A A^T), s_acc = c, E = A and
 //            s_e = b it produces B = b A + c A A.
@@ -17,12 +19,14 @@
 //            X' = a X + B X with the combination done on the fp32
 //            accumulator before the single bf16 rounding.
 //
-// Structure: a persistent grid (one CTA per SM) walks a host-built tile list
+// Structure: a persistent grid (one CTA per SM, in clusters of two that share
+// the B operand through TMA multicast) walks a host-built tile list
 // covering every matrix of every shape group in the batch. Warp 0 issues TMA
 // loads into a ring of shared-memory stages, one thread of warp 1 issues
 // tcgen05.mma into a double-buffered fp32 accumulator in tensor memory, and
-// warps 2-5 drain the accumulator (tcgen05.ld), apply the epilogue and store
-// bf16 to global memory. Every wait is bounded (see mbar_wait_bounded).
+// warps 2-9 drain the accumulator (tcgen05.ld), apply the epilogue and store
+// bf16 to global memory. A host-built schedule gives each CTA its own list of
+// tiles, balanced by contraction length. Every wait is bounded (see mbar_wait_bounded).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -32,7 +36,8 @@
 namespace muon {
 
 constexpr int kMaxGroups = 6;   // shape groups served by one launch
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
+constexpr int kEpilogueThreads = 256;
 
 struct GemmGroup {
   uint16_t* out;          // bf16 [count][rows_out][ld_out]
@@ -47,7 +52,9 @@ struct GemmArgs {
   CUtensorMap map_b[kMaxGroups];  // operand B: Gram: same as A; combine: MN-major, box 64 x 64
   GemmGroup grp[kMaxGroups];
   const int4* tiles;              // {group, matrix within group, tile row, tile col}
+  const int* cta_begin;           // CTA b walks tiles[cta_begin[b] .. cta_begin[b+1])
   int num_tiles;
+  int grid;                       // CTAs launched (entries of cta_begin minus one)
   int num_groups;
   float s_acc;
   float s_e;
@@ -87,6 +94,19 @@ __device__ __forceinline__ void add_row32(float (&v)[32], const uint16_t* e, int
   }
 }
 
+// v[0..31] += s * (32 bf16 values held in four 16-byte registers).
+__device__ __forceinline__ void add_regs32(float (&v)[32], const uint4 (&w4)[4], float s) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t ww[4] = {w4[q].x, w4[q].y, w4[q].z, w4[q].w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      v[q * 8 + 2 * h] += s * bf16_bits_to_float(ww[h] & 0xFFFFu);
+      v[q * 8 + 2 * h + 1] += s * bf16_bits_to_float(ww[h] >> 16);
+    }
+  }
+}
+
 __device__ __forceinline__ void store_row32(uint16_t* o, const float (&v)[32], int limit) {
   if (limit >= 32) {
     uint4* p = reinterpret_cast<uint4*>(o);
@@ -123,14 +143,21 @@ struct GemmShape {
   static constexpr uint32_t SMEM_BYTES = 1024 + kStages * (A_BYTES + B_BYTES) + BAR_BYTES;
 };
 
-template <bool kGram, int kBN, int kStages>
+// kCluster = 2: the two CTAs of a cluster take tile rows I and I+1 of the same
+// tile column, so they need the same B block. Each loads its own A and one
+// half of B, and multicasts that half into both CTAs' shared memory. A stage
+// is refilled only when both CTAs' MMAs have released it, so every MMA commit
+// of a stage arrives on that stage's empty barrier in both CTAs.
+template <bool kGram, int kBN, int kStages, int kCluster>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs args) {
   using S = GemmShape<kGram, kBN, kStages>;
   constexpr int BM = S::BM, BK = S::BK;
   constexpr uint32_t A_BYTES = S::A_BYTES, B_BYTES = S::B_BYTES;
   constexpr uint32_t kIdesc = instr_desc_bf16(BM, kBN, !kGram);
-  static_assert(kBN == 128 || kBN == 256, "tile width");
-  static_assert(S::TMEM_COLS == 256 || S::TMEM_COLS == 512, "TMEM allocation must be a power of two");
+  constexpr uint16_t kPairMask = 0x3;
+  static_assert(kBN == 256, "tile width");
+  static_assert(kCluster == 1 || kCluster == 2, "cluster size");
+  static_assert(S::TMEM_COLS == 512, "TMEM allocation must be a power of two");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -143,23 +170,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = kCluster == 2 ? static_cast<int>(cluster_cta_rank()) : 0;
+  const int list = blockIdx.x / kCluster;  // this CTA's (or cluster's) tile list
+  const int t_begin = args.cta_begin[list], t_end = args.cta_begin[list + 1];
   const uint32_t bar0 = smem_u32(bars);
-  // full[s]: stage s loaded; empty[s]: stage s consumed by the MMAs;
+  // full[s]: stage s loaded; empty[s]: stage s consumed by the MMAs (of both CTAs);
   // tfull[a]: accumulator a complete; tempty[a]: accumulator a drained; drain: abort path.
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto full_bar = [&](int st) { return bar0 + 8u * st; };
+  auto empty_bar = [&](int st) { return bar0 + 8u * (kStages + st); };
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(full_bar(st), 1);
+      mbar_init(empty_bar(st), kCluster);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 128);
+      mbar_init(tempty_bar(a), kEpilogueThreads);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -177,6 +207,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
+  if (kCluster > 1) cluster_sync_all();  // the peer's barriers exist before anything is sent to them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -187,13 +218,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       uint32_t phase = 0;
       uint32_t armed = 0;        // bit s: stage s has a load in flight or landed
       uint32_t armed_parity = 0; // bit s: parity of that load's phase
-      for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+      for (int t = t_begin; t < t_end; ++t) {
         const int4 td = args.tiles[t];
+        const int I = td.z + rank;
         const GemmGroup& G = args.grp[td.x];
         const CUtensorMap* ma = &args.map_a[td.x];
         const CUtensorMap* mb = &args.map_b[td.x];
-        const bool diag = kGram && (td.z == td.w);
-        const uint32_t bytes = diag ? A_BYTES : A_BYTES + B_BYTES;
+        // Gram tiles whose 128 A rows lie inside the 256-row B block read A from B's copy.
+        const bool a_in_b = kGram && ((I >> 1) == td.w);
+        const uint32_t bytes = a_in_b ? B_BYTES : A_BYTES + B_BYTES;
         bool ok = true;
         for (int kb = 0; kb < G.nk; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) {
@@ -203,14 +236,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           mbar_arrive_expect_tx(full_bar(stage), bytes);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          tma_load_3d(smem_u32(sA + stage * A_BYTES), ma, full_bar(stage), kb * BK, td.z * BM, td.y);
+          if (!a_in_b) tma_load_3d(smem_u32(sA + stage * A_BYTES), ma, full_bar(stage), kb * BK, I * BM, td.y);
           const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
-          if (kGram) {
-            if (!diag) tma_load_3d(b_dst, mb, full_bar(stage), kb * BK, td.w * kBN, td.y);
-          } else {
+          // B in boxes: Gram two boxes of 128 rows (K-major), combine four boxes of 64 columns (MN-major).
+          constexpr int kBoxes = kGram ? 2 : 4;
+          constexpr uint32_t kBoxBytes = B_BYTES / kBoxes;
 #pragma unroll
-            for (int c = 0; c < kBN / 64; ++c)
-              tma_load_3d(b_dst + c * 8192u, mb, full_bar(stage), td.w * kBN + c * 64, kb * BK, td.y);
+          for (int c = 0; c < kBoxes; ++c) {
+            if (kCluster == 2 && (c * 2 / kBoxes) != rank) continue;  // the peer sends this half
+            const int x = kGram ? kb * BK : td.w * kBN + c * 64;
+            const int y = kGram ? td.w * kBN + c * 128 : kb * BK;
+            if (kCluster == 2)
+              tma_load_3d_multicast(b_dst + c * kBoxBytes, mb, full_bar(stage), x, y, td.y, kPairMask);
+            else
+              tma_load_3d(b_dst + c * kBoxBytes, mb, full_bar(stage), x, y, td.y);
           }
           if (++stage == kStages) {
             stage = 0;
@@ -221,8 +260,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       }
       if (*abort_flag) {
         // Let loads already issued land before the CTA's shared memory is released.
-        for (int s = 0; s < kStages; ++s)
-          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_parity >> s) & 1u);
+        for (int st = 0; st < kStages; ++st)
+          if (armed & (1u << st)) mbar_wait_drain(full_bar(st), (armed_parity >> st) & 1u);
       }
     }
   } else if (warp == 1) {
@@ -233,10 +272,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       int acc = 0;
       uint32_t acc_phase = 0;
       bool issued = false;
-      for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+      for (int t = t_begin; t < t_end; ++t) {
         const int4 td = args.tiles[t];
+        const int I = td.z + rank;
         const int nk = args.grp[td.x].nk;
-        const bool diag = kGram && (td.z == td.w);
+        const bool a_in_b = kGram && ((I >> 1) == td.w);
         if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
@@ -247,8 +287,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
-          const uint32_t b_addr = diag ? a_addr : smem_u32(sB + stage * B_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+          const uint32_t a_addr = a_in_b ? b_addr + static_cast<uint32_t>(I & 1) * A_BYTES
+                                         : smem_u32(sA + stage * A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             // K-major: the next 16 k-values are 32 bytes further along each 128-byte row.
@@ -259,7 +300,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             mma_bf16_ss(d_tmem, a_desc, b_desc, kIdesc, (kb | k) != 0 ? 1u : 0u);
           }
           issued = true;
-          mma_commit(empty_bar(stage));
+          if (kCluster == 2)
+            mma_commit_multicast(empty_bar(stage), kPairMask);
+          else
+            mma_commit(empty_bar(stage));
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -279,34 +323,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Eight warps, two per TMEM lane quarter; each drains half of the tile's columns.
+    constexpr int kHalfCols = kBN / 2;
+    constexpr int kChunks = kHalfCols / 32;
     const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter .. +31
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+    for (int t = t_begin; t < t_end; ++t) {
       const int4 td = args.tiles[t];
+      const int I = td.z + rank;
       const GemmGroup& G = args.grp[td.x];
-      if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
-      tc_fence_after();
-      const int row = td.z * BM + row_in_tile;
+      const int row = I * BM + row_in_tile;
       const bool row_ok = row < G.rows_out;
       const int64_t ld = G.ld_out;
       uint16_t* out = G.out + static_cast<int64_t>(td.y) * G.mat_stride;
       const uint16_t* e = G.e ? G.e + static_cast<int64_t>(td.y) * G.mat_stride : nullptr;
-      const bool mirror = kGram && (td.z != td.w);
-#pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
+      // Gram: this half is the 128x128 block (tile row I, block column 2*td.w + half). Blocks
+      // below the diagonal are skipped (their transposes come from other tiles), blocks above it are
+      // stored twice (in place and mirrored), the diagonal block once.
+      const int block_col = 2 * td.w + half;
+      const bool skip = kGram && (block_col < I);
+      const bool mirror = kGram && (block_col > I);
+      const int col_base = td.w * kBN + half * kHalfCols;
+      // The addend does not depend on the accumulator: load all of it while this tile's MMAs run.
+      uint4 ev[kChunks][4];
+      if (e && row_ok && !skip) {
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+          if (G.cols_out - (col_base + c * 32) >= 32) {
+            const uint4* p = reinterpret_cast<const uint4*>(e + row * ld + col_base + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ev[c][q] = __ldg(p + q);
+          }
+        }
+      }
+      if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < (skip ? 0 : kChunks); ++c) {
         uint32_t r[32];
-        tmem_load_32cols(tmem_base + lane_field + static_cast<uint32_t>(acc * kBN + c * 32), r);
+        tmem_load_32cols(tmem_base + lane_field + static_cast<uint32_t>(acc * kBN + half * kHalfCols + c * 32), r);
         tmem_load_wait();
-        const int col0 = td.w * kBN + c * 32;
+        const int col0 = col_base + c * 32;
         const int limit = G.cols_out - col0;
         float v[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = args.s_acc * __uint_as_float(r[k]);
         if (row_ok && limit > 0) {
-          if (e) add_row32(v, e + row * ld + col0, limit, args.s_e);
+          if (e) {
+            if (limit >= 32)
+              add_regs32(v, ev[c], args.s_e);
+            else
+              add_row32(v, e + row * ld + col0, limit, args.s_e);
+          }
           store_row32(out + row * ld + col0, v, limit);
           if (mirror) {
             // Transposed copy: for a fixed column the 32 lanes write 32 consecutive elements.
@@ -326,6 +398,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   }
 
   __syncthreads();
+  // No CTA leaves while its peer may still deliver loads or MMA-commit arrivals into it.
+  if (kCluster > 1) cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();

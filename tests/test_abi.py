@@ -89,8 +89,8 @@ def test_plan_stats_gpt2_124m():
     shapes = [(768, 768)] * 4 + [(768, 3072), (3072, 768)]
     s = mu.plan_stats(shapes * 12)
     assert s["groups"] == 2
-    # 768 = 6 tiles of 128: 21 upper-triangle Gram tiles per matrix
-    assert s["gram_tiles"] == 72 * 21
+    # 768 = 6 row tiles of 128 and 3 column tiles of 256: 2 + 4 + 6 = 12 Gram tiles reach the upper triangle
+    assert s["gram_tiles"] == 72 * 12
     # combine: 6 row tiles x (3 or 12) column tiles of 256
     assert s["combine_tiles"] == 48 * 6 * 3 + 24 * 6 * 12
     n = 768
@@ -102,7 +102,15 @@ def test_plan_stats_gpt2_124m():
 def test_plan_stats_ragged_and_c():
     s = mu.plan_stats([(130, 70), (70, 130), (0, 5)], with_c=True)
     assert s["groups"] == 1
-    assert s["gram_tiles"] == 2 * 2 * 1  # one 1x1 upper triangle per matrix, doubled for the A A pass
+    assert s["gram_tiles"] == 2 * 2 * 1  # one tile per matrix, doubled for the A A pass
+    # 1024 = 8 row tiles, 4 column tiles: 2 + 4 + 6 + 8; 4096: 32 row tiles, 16 column tiles
+    assert mu.plan_stats([(1024, 1024)])["gram_tiles"] == 20
+    assert mu.plan_stats([(4096, 16384)])["gram_tiles"] == sum(min(2 * j + 2, 32) for j in range(16))
     assert s["combine_tiles"] == 2
     n, m = 70, 130
     assert s["flops_per_iter"] == pytest.approx(2 * (n * (n + 1) * m + 2 * n * n * m + n * n * (n + 1)))
+
+
+def test_selftest_wait_rejects_bad_limits_without_a_handle():
+    lib = mu.load_library()
+    assert lib.muon_selftest_wait(None, 50_000_000, None) == MUON_ERR_INVALID

@@ -16,7 +16,7 @@ def test_kernel_work_matches_plan_stats():
     w = wl.GPT2_124M
     work = bench.kernel_work(w)
     s = mu.plan_stats(w.shapes)
-    assert work["gram_xxt"][1] + work["combine_ax_bx"][1] == pytest.approx(s["flops_per_iter"])
+    assert work["gram_xxt"][1] + work["combine_ax_bx"][1] == pytest.approx(5 * s["flops_per_iter"])
     assert bench.step_flops(w) == pytest.approx(5 * s["flops_per_iter"])
     assert work["momentum_norm"] == ("bytes", 84934656 * 12.0)
     assert work["update"] == ("bytes", 84934656 * 6.0)

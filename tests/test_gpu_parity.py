@@ -178,3 +178,16 @@ def test_step_f32_grads_config1(muon):
     # distance to the SVD polar factor is a reported number (about 0.5 after 5 steps), not a pass/fail bound
     u, _, vt = np.linalg.svd(g.astype(np.float64), full_matrices=False)
     assert abs(rel_f(got, u @ vt) - rel_f(o, u @ vt)) < 0.02
+
+
+def test_bounded_wait_expiry_is_reported_and_recoverable(muon):
+    """A device wait that nothing satisfies gives up after its limit and raises MUON_ERR_TIMEOUT, and the
+    context keeps working (failure detection without a fault or a hang)."""
+    from muon_newton_schulz_09_b300 import MUON_ERR_TIMEOUT, MUON_OK
+    assert muon.get_error() == MUON_OK
+    muon.selftest_wait(50_000_000)
+    assert muon.get_error() == MUON_ERR_TIMEOUT
+    assert muon.get_error() == MUON_OK  # reading clears the flag
+    _, xs = inputs_for([(256, 384)], "bf16", seed=16)
+    got = run_orth(muon, xs, "bf16", "f32", 5, CUBIC)
+    assert rel_f(got[0], oracle.orthogonalize(xs[0], 5, CUBIC)) < TOL
