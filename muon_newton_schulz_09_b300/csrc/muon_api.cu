@@ -146,7 +146,8 @@ struct GemmBatch {           // up to kMaxGroups groups served by one launch
   int4* comb_tiles = nullptr;
   int* comb_begin = nullptr;
   int num_comb_tiles = 0, comb_grid = 0;
-  GemmArgs gram[2];          // X_t -> (b A or A), t parity
+  GemmArgs gram[2];          // X_t -> b A in the B buffer, t parity
+  GemmArgs gram_to_a[2];     // X_t -> A in the A buffer (c != 0)
   GemmArgs gram_aa;          // A -> c A A + b A
   GemmArgs comb[2];          // (B, X_t) -> X_{t+1}
 };
@@ -248,14 +249,15 @@ struct ProfScope {
 };
 
 bool encode_map(muon_handle h, CUtensorMap* map, void* base, int64_t inner, int64_t rows, int64_t count,
-                int64_t ld, int box_inner, int box_rows) {
+                int64_t ld, int box_inner, int box_rows, bool swizzle = true) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(count)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(rows * ld * 2)};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -471,6 +473,8 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
       B.comb[t].grid = B.comb_grid;
     }
     B.gram_aa = B.gram[0];
+    B.gram_to_a[0] = B.gram[0];
+    B.gram_to_a[1] = B.gram[1];
     for (int gi = 0; gi < B.num_groups; ++gi) {
       const Group& g = P.groups[B.first_group + gi];
       uint8_t* xb[2] = {P.ws + g.x_off[0], P.ws + g.x_off[1]};
@@ -481,19 +485,30 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
         // Gram on X_t: both operands are rows of X_t (K-major), output n x n.
         ok &= encode_map(h, &B.gram[t].map_a[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 128);
         B.gram[t].map_b[gi] = B.gram[t].map_a[gi];
-        B.gram[t].grp[gi] = GemmGroup{pbuf, nullptr, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
+        ok &= encode_map(h, &B.gram[t].map_out[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 32);
+        ok &= encode_map(h, &B.gram[t].map_mirror[gi], pbuf, g.n, g.n, g.count, g.ld_p, 32, 64, false);
+        B.gram[t].grp[gi] = GemmGroup{nullptr, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
                                       static_cast<int>(g.ld_p), static_cast<int>(ceil_div(g.m, 64))};
-        // Combine: A operand = B (n x n, K-major), B operand = X_t MN-major, out = X_{1-t}.
+        // The same Gram writing A = X X^T into the A buffer (first pass when c != 0).
+        B.gram_to_a[t].map_a[gi] = B.gram[t].map_a[gi];
+        B.gram_to_a[t].map_b[gi] = B.gram[t].map_b[gi];
+        B.gram_to_a[t].grp[gi] = B.gram[t].grp[gi];
+        ok &= encode_map(h, &B.gram_to_a[t].map_out[gi], abuf, g.n, g.n, g.count, g.ld_p, 64, 32);
+        ok &= encode_map(h, &B.gram_to_a[t].map_mirror[gi], abuf, g.n, g.n, g.count, g.ld_p, 32, 64, false);
+        // Combine: A operand = B (n x n, K-major), B operand = X_t MN-major, out = X_{1-t}, addend X_t.
         ok &= encode_map(h, &B.comb[t].map_a[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 128);
         ok &= encode_map(h, &B.comb[t].map_b[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 64);
-        B.comb[t].grp[gi] = GemmGroup{reinterpret_cast<uint16_t*>(xb[1 - t]), reinterpret_cast<uint16_t*>(xb[t]),
-                                      g.n * g.ld_x, static_cast<int>(g.n), static_cast<int>(g.m),
-                                      static_cast<int>(g.ld_x), static_cast<int>(ceil_div(g.n, 64))};
+        ok &= encode_map(h, &B.comb[t].map_out[gi], xb[1 - t], g.m, g.n, g.count, g.ld_x, 64, 32);
+        B.comb[t].grp[gi] = GemmGroup{reinterpret_cast<uint16_t*>(xb[t]), g.n * g.ld_x, static_cast<int>(g.n),
+                                      static_cast<int>(g.m), static_cast<int>(g.ld_x),
+                                      static_cast<int>(ceil_div(g.n, 64))};
       }
       // A A pass: operands are rows of A (symmetric), addend A, output B.
       ok &= encode_map(h, &B.gram_aa.map_a[gi], abuf, g.n, g.n, g.count, g.ld_p, 64, 128);
       B.gram_aa.map_b[gi] = B.gram_aa.map_a[gi];
-      B.gram_aa.grp[gi] = GemmGroup{pbuf, abuf, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
+      ok &= encode_map(h, &B.gram_aa.map_out[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 32);
+      ok &= encode_map(h, &B.gram_aa.map_mirror[gi], pbuf, g.n, g.n, g.count, g.ld_p, 32, 64, false);
+      B.gram_aa.grp[gi] = GemmGroup{abuf, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
                                     static_cast<int>(g.ld_p), static_cast<int>(ceil_div(g.n, 64))};
       if (!ok) {
         free_plan(&P);
@@ -737,11 +752,7 @@ muon_status run_iterations(muon_handle h, const Plan& P, int steps, float a, flo
         g.s_e = 0.f;
         st = launch_gemm<true, kGramBN, kGramStages>(h, g, s, K_GRAM);
       } else {
-        GemmArgs g = B.gram[t];  // A = X X^T into the A buffer
-        for (int gi = 0; gi < g.num_groups; ++gi) {
-          const Group& grp = P.groups[B.first_group + gi];
-          g.grp[gi].out = reinterpret_cast<uint16_t*>(P.ws + grp.a_off);
-        }
+        GemmArgs g = B.gram_to_a[t];  // A = X X^T into the A buffer
         g.s_acc = 1.f;
         g.s_e = 0.f;
         st = launch_gemm<true, kGramBN, kGramStages>(h, g, s, K_GRAM);

@@ -40,9 +40,8 @@ constexpr int kGemmThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 constexpr int kEpilogueThreads = 256;
 
 struct GemmGroup {
-  uint16_t* out;          // bf16 [count][rows_out][ld_out]
-  const uint16_t* e;      // bf16 addend in the same layout as out, or nullptr
-  int64_t mat_stride;     // elements between consecutive matrices of out and e
+  const uint16_t* e;      // bf16 addend [count][rows_out][ld_out] (the output's layout), or nullptr
+  int64_t mat_stride;     // elements between consecutive matrices of e
   int rows_out, cols_out, ld_out;
   int nk;                 // number of 64-wide k-blocks of the contraction
 };
@@ -50,6 +49,8 @@ struct GemmGroup {
 struct GemmArgs {
   CUtensorMap map_a[kMaxGroups];  // operand A: K-major, box 64 x 128
   CUtensorMap map_b[kMaxGroups];  // operand B: Gram: same as A; combine: MN-major, box 64 x 64
+  CUtensorMap map_out[kMaxGroups];     // output, box 64 columns x 32 rows, 128-byte swizzle
+  CUtensorMap map_mirror[kMaxGroups];  // Gram output again, box 32 columns x 64 rows, no swizzle
   GemmGroup grp[kMaxGroups];
   const int4* tiles;              // {group, matrix within group, tile row, tile col}
   const int* cta_begin;           // CTA b walks tiles[cta_begin[b] .. cta_begin[b+1])
@@ -138,9 +139,10 @@ struct GemmShape {
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = kBN * BK * 2;
   static constexpr uint32_t TMEM_COLS = 2 * kBN;
+  static constexpr uint32_t STAGING_BYTES = 8 * 4096;  // one 32 x 64 bf16 box per epilogue warp
   static constexpr uint32_t BAR_BYTES = 8 * (2 * kStages + 5) + 16;
   // 1024 bytes of slack to align the swizzled tiles to 1024.
-  static constexpr uint32_t SMEM_BYTES = 1024 + kStages * (A_BYTES + B_BYTES) + BAR_BYTES;
+  static constexpr uint32_t SMEM_BYTES = 1024 + kStages * (A_BYTES + B_BYTES) + STAGING_BYTES + BAR_BYTES;
 };
 
 // kCluster = 2: the two CTAs of a cluster take tile rows I and I+1 of the same
@@ -164,7 +166,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * B_BYTES);
+  uint8_t* staging = sB + kStages * B_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + S::STAGING_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -199,6 +202,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     for (int g = 0; g < args.num_groups; ++g) {
       tma_prefetch_map(&args.map_a[g]);
       tma_prefetch_map(&args.map_b[g]);
+      tma_prefetch_map(&args.map_out[g]);
+      if (kGram) tma_prefetch_map(&args.map_mirror[g]);
     }
   }
   if (warp == 1) {
@@ -323,13 +328,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Eight warps, two per TMEM lane quarter; each drains half of the tile's columns.
+    // Eight warps, two per TMEM lane quarter; each drains half of the tile's columns, 64 at a
+    // time, through its own 4 KB staging box in shared memory and a TMA store.
     constexpr int kHalfCols = kBN / 2;
     constexpr int kChunks = kHalfCols / 32;
     const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter .. +31
     const int half = (warp - 2) >> 2;
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+    uint8_t* stg = staging + (warp - 2) * 4096;
+    const uint32_t stg_addr = smem_u32(stg);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = t_begin; t < t_end; ++t) {
@@ -339,7 +347,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const int row = I * BM + row_in_tile;
       const bool row_ok = row < G.rows_out;
       const int64_t ld = G.ld_out;
-      uint16_t* out = G.out + static_cast<int64_t>(td.y) * G.mat_stride;
       const uint16_t* e = G.e ? G.e + static_cast<int64_t>(td.y) * G.mat_stride : nullptr;
       // Gram: this half is the 128x128 block (tile row I, block column 2*td.w + half). Blocks
       // below the diagonal are skipped (their transposes come from other tiles), blocks above it are
@@ -362,29 +369,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       }
       if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
       tc_fence_after();
+      if (!skip) {
 #pragma unroll
-      for (int c = 0; c < (skip ? 0 : kChunks); ++c) {
-        uint32_t r[32];
-        tmem_load_32cols(tmem_base + lane_field + static_cast<uint32_t>(acc * kBN + half * kHalfCols + c * 32), r);
-        tmem_load_wait();
-        const int col0 = col_base + c * 32;
-        const int limit = G.cols_out - col0;
-        float v[32];
+        for (int box = 0; box < kChunks / 2; ++box) {
+          uint32_t packed[32];  // this thread's 64 output values of the box, as bf16 pairs
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = args.s_acc * __uint_as_float(r[k]);
-        if (row_ok && limit > 0) {
-          if (e) {
-            if (limit >= 32)
-              add_regs32(v, ev[c], args.s_e);
-            else
-              add_row32(v, e + row * ld + col0, limit, args.s_e);
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = box * 2 + cc;
+            uint32_t r[32];
+            tmem_load_32cols(tmem_base + lane_field + static_cast<uint32_t>(acc * kBN + half * kHalfCols + c * 32), r);
+            tmem_load_wait();
+            float v[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = args.s_acc * __uint_as_float(r[k]);
+            if (e && row_ok) {
+              const int limit = G.cols_out - (col_base + c * 32);
+              if (limit >= 32)
+                add_regs32(v, ev[c], args.s_e);
+              else if (limit > 0)
+                add_row32(v, e + row * ld + col_base + c * 32, limit, args.s_e);
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) packed[cc * 16 + k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
           }
-          store_row32(out + row * ld + col0, v, limit);
-          if (mirror) {
-            // Transposed copy: for a fixed column the 32 lanes write 32 consecutive elements.
+          // The staging box is free once the previous store from it has been read.
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+          // Row `lane` of a 32 x 64 box: eight 16-byte chunks, chunk j at position j ^ (lane & 7).
 #pragma unroll
-            for (int k = 0; k < 32; ++k)
-              if (k < limit) out[static_cast<int64_t>(col0 + k) * ld + row] = to_bf16_bits(v[k]);
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t off = static_cast<uint32_t>(lane) * 128u + static_cast<uint32_t>((j ^ (lane & 7)) * 16);
+            *reinterpret_cast<uint4*>(stg + off) =
+                make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int x0 = col_base + box * 64, y0 = I * BM + quarter * 32;
+          if (lane == 0) {
+            tma_store_3d(&args.map_out[td.x], stg_addr, x0, y0, td.y);
+            bulk_commit_group();
+          }
+          if (mirror) {
+            // The transposed box: 64 rows (this box's columns) x 32 columns (the warp's rows), unswizzled.
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              reinterpret_cast<uint16_t*>(stg + (2 * k) * 64)[lane] = static_cast<uint16_t>(packed[k] & 0xFFFFu);
+              reinterpret_cast<uint16_t*>(stg + (2 * k + 1) * 64)[lane] = static_cast<uint16_t>(packed[k] >> 16);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&args.map_mirror[td.x], stg_addr, y0, x0, td.y);
+              bulk_commit_group();
+            }
           }
         }
       }
@@ -395,6 +434,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait_group0();  // every store of this warp has reached global memory
   }
 
   __syncthreads();
