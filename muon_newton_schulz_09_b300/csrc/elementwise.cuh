@@ -35,24 +35,6 @@ __device__ __forceinline__ uint16_t f_to_bf16(float x) {
 }
 
 template <bool kF32>
-__device__ __forceinline__ void load8(const void* base, int64_t idx, float (&v)[8]) {
-  if (kF32) {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx);
-    const float4 a = __ldg(p), b = __ldg(p + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  } else {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + idx));
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      v[2 * h] = __uint_as_float(ww[h] << 16);
-      v[2 * h + 1] = __uint_as_float(ww[h] & 0xFFFF0000u);
-    }
-  }
-}
-
-template <bool kF32>
 __device__ __forceinline__ void store8(void* base, int64_t idx, const float (&v)[8]) {
   if (kF32) {
     float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + idx);
@@ -64,6 +46,43 @@ __device__ __forceinline__ void store8(void* base, int64_t idx, const float (&v)
     for (int h = 0; h < 4; ++h)
       w[h] = static_cast<uint32_t>(f_to_bf16(v[2 * h])) | (static_cast<uint32_t>(f_to_bf16(v[2 * h + 1])) << 16);
     *reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + idx) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Eight consecutive elements in their storage form (one or two 16-byte words), so that every
+// load of a thread can be in flight before any of them is unpacked.
+template <bool kF32>
+struct Raw8 {
+  uint4 w[kF32 ? 2 : 1];
+};
+
+template <bool kF32>
+__device__ __forceinline__ Raw8<kF32> ld_raw8(const void* base, int64_t idx) {
+  Raw8<kF32> r;
+  if constexpr (kF32) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(base) + idx);
+    r.w[0] = p[0];
+    r.w[1] = p[1];
+  } else {
+    r.w[0] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + idx);
+  }
+  return r;
+}
+
+template <bool kF32>
+__device__ __forceinline__ void unpack8(const Raw8<kF32>& r, float (&v)[8]) {
+  if constexpr (kF32) {
+    v[0] = __uint_as_float(r.w[0].x); v[1] = __uint_as_float(r.w[0].y);
+    v[2] = __uint_as_float(r.w[0].z); v[3] = __uint_as_float(r.w[0].w);
+    v[4] = __uint_as_float(r.w[1].x); v[5] = __uint_as_float(r.w[1].y);
+    v[6] = __uint_as_float(r.w[1].z); v[7] = __uint_as_float(r.w[1].w);
+  } else {
+    const uint32_t ww[4] = {r.w[0].x, r.w[0].y, r.w[0].z, r.w[0].w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      v[2 * h] = __uint_as_float(ww[h] << 16);
+      v[2 * h + 1] = __uint_as_float(ww[h] & 0xFFFF0000u);
+    }
   }
 }
 
@@ -112,7 +131,7 @@ struct MomMat {
   uint16_t* u;         // bf16 u, rows x cols contiguous
   int64_t ld_g, ld_buf;
   int rows, cols;
-  int vec_ok;          // 16-byte vector path allowed
+  int vec_ok;          // contiguous (ld == cols), cols % 8 == 0 and 16-byte aligned: vector path
   int block_begin;     // first block of this matrix in the launch
   int nchunks;         // blocks of this matrix = partial sums
   float* partial;      // nchunks partial sums of u^2
@@ -129,7 +148,7 @@ struct MomArgs {
 };
 
 template <bool kStep, bool kSrcF32>
-__global__ void __launch_bounds__(kEwThreads) momentum_norm_kernel(const __grid_constant__ MomArgs a) {
+__global__ void __launch_bounds__(kEwThreads, kSrcF32 ? 3 : 4) momentum_norm_kernel(const __grid_constant__ MomArgs a) {
   const int j = owner_of_block(a.m, a.count, static_cast<int>(blockIdx.x));
   const MomMat& M = a.m[j];
   const int chunk = static_cast<int>(blockIdx.x) - M.block_begin;
@@ -141,38 +160,39 @@ __global__ void __launch_bounds__(kEwThreads) momentum_norm_kernel(const __grid_
   float ss = 0.f;
 
   if (M.vec_ok) {
+    // Vector path: contiguous rows (ld == cols), 16-byte aligned, so element e sits at offset e.
     constexpr int V = kFlatChunk / (kEwThreads * 8);
-    float g[V][8], b[V][8];
-    int64_t gi[V], bi[V], e[V];
+    Raw8<kSrcF32> gr[V];
+    Raw8<true> br[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      e[v] = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
-      if (e[v] < e1) {
-        const int64_t row = e[v] / cols, col = e[v] - row * cols;
-        gi[v] = row * M.ld_g + col;
-        bi[v] = row * M.ld_buf + col;
-        load8<kSrcF32>(M.g, gi[v], g[v]);
-        if (kStep) load8<true>(M.buf, bi[v], b[v]);
+      const int64_t e = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
+      if (e < e1) {
+        gr[v] = ld_raw8<kSrcF32>(M.g, e);
+        if (kStep) br[v] = ld_raw8<true>(M.buf, e);
       }
     }
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      if (e[v] < e1) {
-        float u[8];
+      const int64_t e = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
+      if (e < e1) {
+        float g[8], b[8], u[8];
+        unpack8<kSrcF32>(gr[v], g);
+        if (kStep) unpack8<true>(br[v], b);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           if (kStep) {
-            const float nb = beta * b[v][k] + g[v][k];
-            b[v][k] = nb;
-            u[k] = a.nesterov ? g[v][k] + beta * nb : nb;
+            const float nb = beta * b[k] + g[k];
+            b[k] = nb;
+            u[k] = a.nesterov ? g[k] + beta * nb : nb;
           } else {
-            u[k] = g[v][k];
+            u[k] = g[k];
           }
           ss += u[k] * u[k];
         }
         if (kStep) {
-          store8<true>(M.buf, bi[v], b[v]);
-          store8<false>(M.u, e[v], u);
+          store8<true>(M.buf, e, b);
+          store8<false>(M.u, e, u);
         }
       }
     }
@@ -244,7 +264,8 @@ struct MapMat {
   int64_t ld_src, ld_dst;
   int sr, sc;          // source rows, cols
   int transposed;
-  int vec_ok;          // both sides allow 16-byte vectors
+  int vec_ok;          // 16-byte vectors allowed: flat path needs ld == cols on both sides,
+                       // transposed path needs both lds % 8 == 0; both need 16-byte aligned pointers
   int block_begin;
   int tiles_c;         // transposed: tiles along the source columns
   float scale;         // kUpdate: lr * s
@@ -256,20 +277,6 @@ struct MapArgs {
   int count;
 };
 
-template <int kMode, bool kSrcF32, bool kDstF32>
-__device__ __forceinline__ void map_apply8(const MapMat& M, float f, const float (&s)[8], int64_t di) {
-  float d[8];
-  if (kMode == kUpdate) {
-    load8<kDstF32>(M.dst, di, d);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) d[k] -= f * s[k];
-  } else {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) d[k] = (kMode == kScale) ? s[k] * f : s[k];
-  }
-  store8<kDstF32>(M.dst, di, d);
-}
-
 template <int kMode, bool kDstF32>
 __device__ __forceinline__ void map_apply1(const MapMat& M, float f, float s, int64_t di) {
   if (kMode == kUpdate)
@@ -278,8 +285,24 @@ __device__ __forceinline__ void map_apply1(const MapMat& M, float f, float s, in
     store1<kDstF32>(M.dst, di, (kMode == kScale) ? s * f : s);
 }
 
+// d = f(s) for eight elements: the old destination values dold are used by kUpdate only.
+template <int kMode>
+__device__ __forceinline__ void map_combine8(float f, const float (&sv)[8], const float (&dold)[8], float (&d)[8]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (kMode == kUpdate)
+      d[k] = dold[k] - f * sv[k];
+    else if (kMode == kScale)
+      d[k] = sv[k] * f;
+    else
+      d[k] = sv[k];
+  }
+}
+
+constexpr int kTileRows = 128;  // transposed path: source tile of 128 rows x 64 columns
+
 template <int kMode, bool kSrcF32, bool kDstF32>
-__global__ void __launch_bounds__(kEwThreads) map_kernel(const __grid_constant__ MapArgs a) {
+__global__ void __launch_bounds__(kEwThreads, 3) map_kernel(const __grid_constant__ MapArgs a) {
   const int j = owner_of_block(a.m, a.count, static_cast<int>(blockIdx.x));
   const MapMat& M = a.m[j];
   const int blk = static_cast<int>(blockIdx.x) - M.block_begin;
@@ -291,21 +314,29 @@ __global__ void __launch_bounds__(kEwThreads) map_kernel(const __grid_constant__
     const int64_t e0 = static_cast<int64_t>(blk) * kFlatChunk;
     const int64_t e1 = min(n, e0 + kFlatChunk);
     if (M.vec_ok) {
+      // Contiguous rows on both sides (ld == cols): element e sits at offset e.
       constexpr int V = kFlatChunk / (kEwThreads * 8);
-      float s[V][8];
-      int64_t e[V], di[V];
+      Raw8<kSrcF32> sr[V];
+      Raw8<kDstF32> dr[V];
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        e[v] = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
-        if (e[v] < e1) {
-          const int64_t row = e[v] / cols, col = e[v] - row * cols;
-          di[v] = row * M.ld_dst + col;
-          load8<kSrcF32>(M.src, row * M.ld_src + col, s[v]);
+        const int64_t e = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
+        if (e < e1) {
+          sr[v] = ld_raw8<kSrcF32>(M.src, e);
+          if (kMode == kUpdate) dr[v] = ld_raw8<kDstF32>(M.dst, e);
         }
       }
 #pragma unroll
-      for (int v = 0; v < V; ++v)
-        if (e[v] < e1) map_apply8<kMode, kSrcF32, kDstF32>(M, f, s[v], di[v]);
+      for (int v = 0; v < V; ++v) {
+        const int64_t e = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
+        if (e < e1) {
+          float sv[8], dold[8], d[8];
+          unpack8<kSrcF32>(sr[v], sv);
+          if (kMode == kUpdate) unpack8<kDstF32>(dr[v], dold);
+          map_combine8<kMode>(f, sv, dold, d);
+          store8<kDstF32>(M.dst, e, d);
+        }
+      }
     } else {
       for (int64_t e = e0 + threadIdx.x; e < e1; e += kEwThreads) {
         const int64_t row = e / cols, col = e - row * cols;
@@ -315,19 +346,39 @@ __global__ void __launch_bounds__(kEwThreads) map_kernel(const __grid_constant__
     return;
   }
 
-  // Transposed: source tile rows r0..r0+63, cols c0..c0+63.
-  __shared__ float tile[kTile][kTile + 1];
-  const int r0 = (blk / M.tiles_c) * kTile;
+  // Transposed: source tile rows r0..r0+127, columns c0..c0+63; destination rows c0..c0+63,
+  // columns r0..r0+127. Both sides move 16-byte vectors along their own rows.
+  __shared__ float tile[kTileRows][kTile + 1];
+  const int r0 = (blk / M.tiles_c) * kTileRows;
   const int c0 = (blk % M.tiles_c) * kTile;
-  const int sub = threadIdx.x >> 3;        // 0..31
-  const int c8 = (threadIdx.x & 7) * 8;    // 0..56
+  // Phase 1 mapping: 8 threads per source row, 32 rows per pass.
+  const int sub = threadIdx.x >> 3;
+  const int c8 = (threadIdx.x & 7) * 8;
+  // Phase 2 mapping: 16 threads per destination row (128 columns), 16 rows per pass.
+  const int drow = threadIdx.x >> 4;
+  const int dcol = (threadIdx.x & 15) * 8;
+  constexpr int P1 = kTileRows / 32, P2 = kTile / 16;
+  Raw8<kSrcF32> sraw[P1];
+  Raw8<kDstF32> draw[P2];
 #pragma unroll
-  for (int p = 0; p < 2; ++p) {
+  for (int p = 0; p < P1; ++p) {
+    const int gr = r0 + p * 32 + sub, gc = c0 + c8;
+    if (M.vec_ok && gr < M.sr && gc + 7 < M.sc) sraw[p] = ld_raw8<kSrcF32>(M.src, static_cast<int64_t>(gr) * M.ld_src + gc);
+  }
+  if (kMode == kUpdate) {
+#pragma unroll
+    for (int p = 0; p < P2; ++p) {
+      const int dr = c0 + p * 16 + drow, dc = r0 + dcol;
+      if (M.vec_ok && dr < M.sc && dc + 7 < M.sr) draw[p] = ld_raw8<kDstF32>(M.dst, static_cast<int64_t>(dr) * M.ld_dst + dc);
+    }
+  }
+#pragma unroll
+  for (int p = 0; p < P1; ++p) {
     const int r = p * 32 + sub;
     const int gr = r0 + r, gc = c0 + c8;
     float v[8];
-    if (gr < M.sr && gc + 7 < M.sc && M.vec_ok) {
-      load8<kSrcF32>(M.src, static_cast<int64_t>(gr) * M.ld_src + gc, v);
+    if (M.vec_ok && gr < M.sr && gc + 7 < M.sc) {
+      unpack8<kSrcF32>(sraw[p], v);
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -338,22 +389,24 @@ __global__ void __launch_bounds__(kEwThreads) map_kernel(const __grid_constant__
     for (int k = 0; k < 8; ++k) tile[r][c8 + k] = v[k];
   }
   __syncthreads();
-  // Destination rows are source columns c0 + cc, destination columns source rows r0 + rr.
 #pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    const int cc = p * 32 + sub;
-    const int dr = c0 + cc, dc = r0 + c8;
+  for (int p = 0; p < P2; ++p) {
+    const int cc = p * 16 + drow;
+    const int dr = c0 + cc, dc = r0 + dcol;
     if (dr >= M.sc) continue;
-    float v[8];
+    float sv[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) v[k] = tile[c8 + k][cc];
+    for (int k = 0; k < 8; ++k) sv[k] = tile[dcol + k][cc];
     const int64_t di = static_cast<int64_t>(dr) * M.ld_dst + dc;
-    if (dc + 7 < M.sr && M.vec_ok) {
-      map_apply8<kMode, kSrcF32, kDstF32>(M, f, v, di);
+    if (M.vec_ok && dc + 7 < M.sr) {
+      float dold[8], d[8];
+      if (kMode == kUpdate) unpack8<kDstF32>(draw[p], dold);
+      map_combine8<kMode>(f, sv, dold, d);
+      store8<kDstF32>(M.dst, di, d);
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (dc + k < M.sr) map_apply1<kMode, kDstF32>(M, f, v[k], di + k);
+        if (dc + k < M.sr) map_apply1<kMode, kDstF32>(M, f, sv[k], di + k);
     }
   }
 }

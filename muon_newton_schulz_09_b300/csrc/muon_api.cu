@@ -601,8 +601,8 @@ muon_status launch_momentum(muon_handle h, const Plan& P, const muon_matrix* src
     M.u = kStep ? x_slot(P, mi, 1) : nullptr;  // u lives in the second X buffer until the scale pass reads it
     M.rows = static_cast<int>(mi.rows);
     M.cols = static_cast<int>(mi.cols);
-    bool vec = (mi.cols % 8 == 0) && (src[j].ld % 8 == 0) && aligned16(src[j].ptr);
-    if (kStep) vec = vec && (buf[j].ld % 8 == 0) && aligned16(buf[j].ptr);
+    bool vec = (mi.cols % 8 == 0) && (src[j].ld == mi.cols) && aligned16(src[j].ptr);
+    if (kStep) vec = vec && (buf[j].ld == mi.cols) && aligned16(buf[j].ptr);
     M.vec_ok = vec ? 1 : 0;
     M.block_begin = blocks;
     M.nchunks = static_cast<int>(mi.nchunks);
@@ -690,13 +690,14 @@ muon_status launch_map(muon_handle h, const Plan& P, const muon_matrix* user, in
       const double sc = h->cfg.scale_lr_by_shape ? std::sqrt(std::max(1.0, double(mi.rows) / double(mi.cols))) : 1.0;
       M.scale = static_cast<float>(double(lr) * sc);
     }
-    const bool vec = (M.sc % 8 == 0 || M.transposed) && (M.ld_src % 8 == 0) && (M.ld_dst % 8 == 0) &&
-                     aligned16(M.src) && aligned16(M.dst);
+    const bool aligned = aligned16(M.src) && aligned16(M.dst);
+    const bool vec = M.transposed ? (aligned && M.ld_src % 8 == 0 && M.ld_dst % 8 == 0)
+                                  : (aligned && M.sc % 8 == 0 && M.ld_src == M.sc && M.ld_dst == M.sc);
     M.vec_ok = vec ? 1 : 0;
     M.block_begin = blocks;
     if (M.transposed) {
       M.tiles_c = static_cast<int>(ceil_div(M.sc, kTile));
-      blocks += static_cast<int>(ceil_div(M.sr, kTile) * M.tiles_c);
+      blocks += static_cast<int>(ceil_div(M.sr, kTileRows) * M.tiles_c);
     } else {
       M.tiles_c = 0;
       blocks += static_cast<int>(ceil_div(static_cast<int64_t>(M.sr) * M.sc, kFlatChunk));

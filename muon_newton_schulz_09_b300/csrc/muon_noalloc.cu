@@ -135,7 +135,7 @@ extern "C" muon_status muon_normalize_noalloc(const muon_matrix* in, const muon_
     N.ld_g = in[j].ld;
     N.rows = static_cast<int>(in[j].rows);
     N.cols = static_cast<int>(in[j].cols);
-    N.vec_ok = (in[j].cols % 8 == 0 && in[j].ld % 8 == 0 && aligned16(in[j].ptr)) ? 1 : 0;
+    N.vec_ok = (in[j].cols % 8 == 0 && in[j].ld == in[j].cols && aligned16(in[j].ptr)) ? 1 : 0;
     N.block_begin = nblocks;
     N.nchunks = nch;
     N.partial = partial + part_off;
@@ -153,7 +153,7 @@ extern "C" muon_status muon_normalize_noalloc(const muon_matrix* in, const muon_
     M.sr = static_cast<int>(in[j].rows);
     M.sc = static_cast<int>(in[j].cols);
     M.transposed = 0;
-    M.vec_ok = (M.sc % 8 == 0 && M.ld_src % 8 == 0 && M.ld_dst % 8 == 0 && aligned16(M.src) && aligned16(M.dst))
+    M.vec_ok = (M.sc % 8 == 0 && M.ld_src == M.sc && M.ld_dst == M.sc && aligned16(M.src) && aligned16(M.dst))
                    ? 1 : 0;
     M.block_begin = mblocks;
     M.inv = inv + k;
