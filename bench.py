@@ -398,9 +398,7 @@ def run_ours(args) -> dict:
     if muon.get_error() != 0:
         raise RuntimeError("device error flag raised during warm-up")
 
-    # ---- timed region: inputs resident in HBM
-    muon.profile_read()
-    muon.profile(True)
+    # ---- timed region: inputs resident in HBM. Nothing but the steps is queued in it.
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
@@ -417,13 +415,32 @@ def run_ours(args) -> dict:
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    muon.profile(False)
-    prof = muon.profile_read()
     elapsed_s = start.elapsed_time(end) / 1e3
     if muon.get_error() != 0:
         raise RuntimeError("device error flag raised during the timed region")
     max_s = reduce_max(elapsed_s)
     value = whole_job_rate(args.steps, world, max_s)
+
+    # ---- the same steps again with every kernel bracketed by CUDA events on the launching
+    # stream (the library's profiling hooks), for per-kernel durations. The events sit between
+    # kernels, so this region runs slightly slower than the one above; its own step time is
+    # reported as ms_per_step_profiled.
+    muon.profile_read()
+    muon.profile(True)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    p0.record(stream)
+    for _ in range(args.steps):
+        step()
+    p1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    muon.profile(False)
+    prof = muon.profile_read()
+    prof_s = p0.elapsed_time(p1) / 1e3
+    if muon.get_error() != 0:
+        raise RuntimeError("device error flag raised during the profiled region")
 
     # ---- end to end through the public API: every step uploads its gradients from pinned host
     # memory and reads the updated parameters (or the orthogonalised output) back to pinned host
@@ -437,7 +454,7 @@ def run_ours(args) -> dict:
 
     # ---- roofline of the dominant kernel, from the per-kernel events of the timed region
     peaks, peak_src = load_peaks()
-    sustained = elapsed_s >= 1.0
+    sustained = prof_s >= 1.0
     tc_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
     work = kernel_work(w)
     kernels = {}
@@ -486,6 +503,7 @@ def run_ours(args) -> dict:
         "e2e": {kk: (round(v, 3) if isinstance(v, float) else v) for kk, v in e2e.items()},
         "gpu_launches": gpu_launches,
         "host_submit_ms_per_step": round(host_s * 1e3, 4),
+        "ms_per_step_profiled": round(prof_s * 1e3 / args.steps, 4),
         "kernel_ms_per_step": round(total_ms / args.steps, 4),
         "clocks": clk.summary(),
         "impl": "ours",

@@ -20,6 +20,8 @@
 
 #include <cstdint>
 
+#include "ptx.cuh"
+
 namespace muon {
 
 constexpr int kEwThreads = 256;
@@ -149,6 +151,7 @@ struct MomArgs {
 
 template <bool kStep, bool kSrcF32>
 __global__ void __launch_bounds__(kEwThreads, kSrcF32 ? 3 : 4) momentum_norm_kernel(const __grid_constant__ MomArgs a) {
+  grid_dependency_wait();
   const int j = owner_of_block(a.m, a.count, static_cast<int>(blockIdx.x));
   const MomMat& M = a.m[j];
   const int chunk = static_cast<int>(blockIdx.x) - M.block_begin;
@@ -303,6 +306,7 @@ constexpr int kTileRows = 128;  // transposed path: source tile of 128 rows x 64
 
 template <int kMode, bool kSrcF32, bool kDstF32>
 __global__ void __launch_bounds__(kEwThreads, 3) map_kernel(const __grid_constant__ MapArgs a) {
+  grid_dependency_wait();
   const int j = owner_of_block(a.m, a.count, static_cast<int>(blockIdx.x));
   const MapMat& M = a.m[j];
   const int blk = static_cast<int>(blockIdx.x) - M.block_begin;

@@ -19,6 +19,7 @@
 #include <cstring>
 #include <map>
 #include <queue>
+#include <utility>
 #include <memory>
 #include <string>
 #include <vector>
@@ -499,6 +500,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
         ok &= encode_map(h, &B.comb[t].map_a[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 128);
         ok &= encode_map(h, &B.comb[t].map_b[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 64);
         ok &= encode_map(h, &B.comb[t].map_out[gi], xb[1 - t], g.m, g.n, g.count, g.ld_x, 64, 32);
+        ok &= encode_map(h, &B.comb[t].map_e[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 32);
         B.comb[t].grp[gi] = GemmGroup{reinterpret_cast<uint16_t*>(xb[t]), g.n * g.ld_x, static_cast<int>(g.n),
                                       static_cast<int>(g.m), static_cast<int>(g.ld_x),
                                       static_cast<int>(ceil_div(g.n, 64))};
@@ -508,6 +510,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
       B.gram_aa.map_b[gi] = B.gram_aa.map_a[gi];
       ok &= encode_map(h, &B.gram_aa.map_out[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 32);
       ok &= encode_map(h, &B.gram_aa.map_mirror[gi], pbuf, g.n, g.n, g.count, g.ld_p, 32, 64, false);
+      ok &= encode_map(h, &B.gram_aa.map_e[gi], abuf, g.n, g.n, g.count, g.ld_p, 64, 32);
       B.gram_aa.grp[gi] = GemmGroup{abuf, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
                                     static_cast<int>(g.ld_p), static_cast<int>(ceil_div(g.n, 64))};
       if (!ok) {
@@ -558,6 +561,25 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // ------------------------------------------------------------------ launches
 
+// Launches with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream finishes, and waits for it in-kernel
+// (griddepcontrol.wait) before touching its outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(block), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 muon_status launch_checked(muon_handle h, const char* what) {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(h, e, what);
@@ -583,9 +605,9 @@ muon_status launch_momentum(muon_handle h, const Plan& P, const muon_matrix* src
     if (a.count == 0) return MUON_OK;
     ProfScope ps(h, kStep ? K_MOMENTUM : K_NORM, s);
     if (f32)
-      momentum_norm_kernel<kStep, true><<<blocks, kEwThreads, 0, s>>>(a);
+      launch_pdl(momentum_norm_kernel<kStep, true>, blocks, kEwThreads, 0, s, a);
     else
-      momentum_norm_kernel<kStep, false><<<blocks, kEwThreads, 0, s>>>(a);
+      launch_pdl(momentum_norm_kernel<kStep, false>, blocks, kEwThreads, 0, s, a);
     a.count = 0;
     blocks = 0;
     return launch_checked(h, "momentum/norm kernel");
@@ -624,13 +646,13 @@ muon_status launch_map_dispatch(muon_handle h, const MapArgs& a, int blocks, boo
                                 cudaStream_t s, int kind) {
   ProfScope ps(h, kind, s);
   if (src_f32 && dst_f32)
-    map_kernel<kMode, true, true><<<blocks, kEwThreads, 0, s>>>(a);
+    launch_pdl(map_kernel<kMode, true, true>, blocks, kEwThreads, 0, s, a);
   else if (src_f32)
-    map_kernel<kMode, true, false><<<blocks, kEwThreads, 0, s>>>(a);
+    launch_pdl(map_kernel<kMode, true, false>, blocks, kEwThreads, 0, s, a);
   else if (dst_f32)
-    map_kernel<kMode, false, true><<<blocks, kEwThreads, 0, s>>>(a);
+    launch_pdl(map_kernel<kMode, false, true>, blocks, kEwThreads, 0, s, a);
   else
-    map_kernel<kMode, false, false><<<blocks, kEwThreads, 0, s>>>(a);
+    launch_pdl(map_kernel<kMode, false, false>, blocks, kEwThreads, 0, s, a);
   return launch_checked(h, "map kernel");
 }
 
@@ -721,8 +743,10 @@ cudaLaunchConfig_t gemm_config(int lists, cudaStream_t s, cudaLaunchAttribute* a
   attr[0].val.clusterDim.x = kCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
@@ -730,7 +754,7 @@ template <bool kGram, int kBN, int kStages>
 muon_status launch_gemm(muon_handle h, const GemmArgs& a, cudaStream_t s, int kind) {
   if (a.num_tiles == 0) return MUON_OK;
   ProfScope ps(h, kind, s);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = gemm_config<kGram, kBN, kStages>(a.grid, s, attr);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kCluster>, a);
   if (e != cudaSuccess) {
@@ -1004,7 +1028,7 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
   // Persistent grids: as many tile lists as clusters (or CTAs) that can be resident at once.
   h->max_lists = h->num_sms / kCluster;
   if (kCluster > 1) {
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     int n1 = 0, n2 = 0;
     cudaLaunchConfig_t c1 = gemm_config<true, kGramBN, kGramStages>(1, nullptr, attr);
     e1 = cudaOccupancyMaxActiveClusters(&n1, ns_gemm_kernel<true, kGramBN, kGramStages, kCluster>, &c1);

@@ -40,7 +40,7 @@ constexpr int kGemmThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 constexpr int kEpilogueThreads = 256;
 
 struct GemmGroup {
-  const uint16_t* e;      // bf16 addend [count][rows_out][ld_out] (the output's layout), or nullptr
+  const uint16_t* e;      // non-null when the epilogue adds s_e * E (E read through map_e)
   int64_t mat_stride;     // elements between consecutive matrices of e
   int rows_out, cols_out, ld_out;
   int nk;                 // number of 64-wide k-blocks of the contraction
@@ -51,6 +51,7 @@ struct GemmArgs {
   CUtensorMap map_b[kMaxGroups];  // operand B: Gram: same as A; combine: MN-major, box 64 x 64
   CUtensorMap map_out[kMaxGroups];     // output, box 64 columns x 32 rows, 128-byte swizzle
   CUtensorMap map_mirror[kMaxGroups];  // Gram output again, box 32 columns x 64 rows, no swizzle
+  CUtensorMap map_e[kMaxGroups];       // addend E, box 64 columns x 32 rows, 128-byte swizzle
   GemmGroup grp[kMaxGroups];
   const int4* tiles;              // {group, matrix within group, tile row, tile col}
   const int* cta_begin;           // CTA b walks tiles[cta_begin[b] .. cta_begin[b+1])
@@ -140,7 +141,7 @@ struct GemmShape {
   static constexpr uint32_t B_BYTES = kBN * BK * 2;
   static constexpr uint32_t TMEM_COLS = 2 * kBN;
   static constexpr uint32_t STAGING_BYTES = 8 * 4096;  // one 32 x 64 bf16 box per epilogue warp
-  static constexpr uint32_t BAR_BYTES = 8 * (2 * kStages + 5) + 16;
+  static constexpr uint32_t BAR_BYTES = 8 * (2 * kStages + 5 + 8) + 16;  // + one addend barrier per epilogue warp
   // 1024 bytes of slack to align the swizzled tiles to 1024.
   static constexpr uint32_t SMEM_BYTES = 1024 + kStages * (A_BYTES + B_BYTES) + STAGING_BYTES + BAR_BYTES;
 };
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   uint8_t* sB = smem + kStages * A_BYTES;
   uint8_t* staging = sB + kStages * B_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + S::STAGING_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5 + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -184,6 +185,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+  auto addend_bar = [&](int w) { return bar0 + 8u * (2 * kStages + 5 + w); };  // epilogue warp w's E box
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
@@ -195,6 +197,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       mbar_init(tempty_bar(a), kEpilogueThreads);
     }
     mbar_init(drain_bar, 1);
+    for (int w = 0; w < 8; ++w) mbar_init(addend_bar(w), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -204,6 +207,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       tma_prefetch_map(&args.map_b[g]);
       tma_prefetch_map(&args.map_out[g]);
       if (kGram) tma_prefetch_map(&args.map_mirror[g]);
+      if (args.grp[g].e) tma_prefetch_map(&args.map_e[g]);
     }
   }
   if (warp == 1) {
@@ -215,6 +219,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   if (kCluster > 1) cluster_sync_all();  // the peer's barriers exist before anything is sent to them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above overlaps the previous kernel's tail; its outputs are read only below.
+  grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -329,25 +335,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   } else {
     // ------------------------------------------------------------ epilogue
     // Eight warps, two per TMEM lane quarter; each drains half of the tile's columns, 64 at a
-    // time, through its own 4 KB staging box in shared memory and a TMA store.
+    // time, through its own 4 KB staging box in shared memory: the addend E (if any) arrives
+    // there by TMA, the result replaces it in place and leaves by a TMA store.
     constexpr int kHalfCols = kBN / 2;
-    constexpr int kChunks = kHalfCols / 32;
+    constexpr int kBoxes = kHalfCols / 64;
     const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter .. +31
     const int half = (warp - 2) >> 2;
-    const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
     uint8_t* stg = staging + (warp - 2) * 4096;
     const uint32_t stg_addr = smem_u32(stg);
+    const uint32_t ebar = addend_bar(warp - 2);
+    uint32_t ephase = 0;
+    bool e_pending = false;  // an addend load was issued and not yet waited for
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = t_begin; t < t_end; ++t) {
       const int4 td = args.tiles[t];
       const int I = td.z + rank;
       const GemmGroup& G = args.grp[td.x];
-      const int row = I * BM + row_in_tile;
-      const bool row_ok = row < G.rows_out;
-      const int64_t ld = G.ld_out;
-      const uint16_t* e = G.e ? G.e + static_cast<int64_t>(td.y) * G.mat_stride : nullptr;
+      const bool has_e = G.e != nullptr;
       // Gram: this half is the 128x128 block (tile row I, block column 2*td.w + half). Blocks
       // below the diagonal are skipped (their transposes come from other tiles), blocks above it are
       // stored twice (in place and mirrored), the diagonal block once.
@@ -355,47 +361,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const bool skip = kGram && (block_col < I);
       const bool mirror = kGram && (block_col > I);
       const int col_base = td.w * kBN + half * kHalfCols;
-      // The addend does not depend on the accumulator: load all of it while this tile's MMAs run.
-      uint4 ev[kChunks][4];
-      if (e && row_ok && !skip) {
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
-          if (G.cols_out - (col_base + c * 32) >= 32) {
-            const uint4* p = reinterpret_cast<const uint4*>(e + row * ld + col_base + c * 32);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ev[c][q] = __ldg(p + q);
-          }
+      const int y0 = I * BM + quarter * 32;
+      // E box `box` into the staging buffer, once the last store from it has been read.
+      auto load_addend = [&](int box) {
+        if (lane == 0) {
+          bulk_wait_group_read0();
+          mbar_arrive_expect_tx(ebar, 4096u);
+          tma_load_3d(stg_addr, &args.map_e[td.x], ebar, col_base + box * 64, y0, td.y);
         }
-      }
+        e_pending = true;
+      };
+      if (has_e && !skip) load_addend(0);  // lands while this tile's MMAs run
       if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
       tc_fence_after();
+      bool ok = true;
       if (!skip) {
 #pragma unroll
-        for (int box = 0; box < kChunks / 2; ++box) {
+        for (int box = 0; box < kBoxes; ++box) {
+          if (has_e && box > 0) load_addend(box);
           uint32_t packed[32];  // this thread's 64 output values of the box, as bf16 pairs
+          float v[64];
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            const int c = box * 2 + cc;
             uint32_t r[32];
-            tmem_load_32cols(tmem_base + lane_field + static_cast<uint32_t>(acc * kBN + half * kHalfCols + c * 32), r);
+            tmem_load_32cols(
+                tmem_base + lane_field + static_cast<uint32_t>(acc * kBN + half * kHalfCols + box * 64 + cc * 32), r);
             tmem_load_wait();
-            float v[32];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = args.s_acc * __uint_as_float(r[k]);
-            if (e && row_ok) {
-              const int limit = G.cols_out - (col_base + c * 32);
-              if (limit >= 32)
-                add_regs32(v, ev[c], args.s_e);
-              else if (limit > 0)
-                add_row32(v, e + row * ld + col_base + c * 32, limit, args.s_e);
-            }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) packed[cc * 16 + k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+            for (int k = 0; k < 32; ++k) v[cc * 32 + k] = args.s_acc * __uint_as_float(r[k]);
           }
-          // The staging box is free once the previous store from it has been read.
-          if (lane == 0) bulk_wait_group_read0();
+          if (has_e) {
+            if (!mbar_wait_bounded(ebar, ephase, abort_flag, args.err)) {
+              ok = false;
+              break;
+            }
+            ephase ^= 1u;
+            e_pending = false;
+            // Row `lane` of the 32 x 64 box: 16-byte chunk j holds columns 8j..8j+7, at position j ^ (lane & 7).
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t off = static_cast<uint32_t>(lane) * 128u + static_cast<uint32_t>((j ^ (lane & 7)) * 16);
+              const uint4 w4 = *reinterpret_cast<const uint4*>(stg + off);
+              const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                v[8 * j + 2 * h] += args.s_e * bf16_bits_to_float(ww[h] & 0xFFFFu);
+                v[8 * j + 2 * h + 1] += args.s_e * bf16_bits_to_float(ww[h] >> 16);
+              }
+            }
+          } else if (lane == 0) {
+            bulk_wait_group_read0();  // the staging box is free once the previous store has read it
+          }
           __syncwarp();
-          // Row `lane` of a 32 x 64 box: eight 16-byte chunks, chunk j at position j ^ (lane & 7).
+#pragma unroll
+          for (int k = 0; k < 32; ++k) packed[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t off = static_cast<uint32_t>(lane) * 128u + static_cast<uint32_t>((j ^ (lane & 7)) * 16);
@@ -404,7 +423,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           }
           fence_proxy_async_smem();
           __syncwarp();
-          const int x0 = col_base + box * 64, y0 = I * BM + quarter * 32;
+          const int x0 = col_base + box * 64;
           if (lane == 0) {
             tma_store_3d(&args.map_out[td.x], stg_addr, x0, y0, td.y);
             bulk_commit_group();
@@ -427,6 +446,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           }
         }
       }
+      if (!ok) break;
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       if (++acc == 2) {
@@ -434,7 +454,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         acc_phase ^= 1u;
       }
     }
-    if (lane == 0) bulk_wait_group0();  // every store of this warp has reached global memory
+    if (lane == 0) {
+      if (e_pending) mbar_wait_drain(ebar, ephase);  // abort path: let the addend load land
+      bulk_wait_group0();  // every store of this warp has reached global memory
+    }
   }
 
   __syncthreads();
