@@ -166,6 +166,15 @@ struct Plan {
   int4* tiles_dev = nullptr;
   int* begin_dev = nullptr;
   uint64_t last_use = 0;
+  // Writing the last combine's result straight into the caller's matrices: tensor maps of the
+  // caller's matrices (re-encoded when a pointer or ld changes) and one argument block per batch.
+  struct UserMap {
+    const void* ptr = nullptr;
+    int64_t ld = -1;
+    CUtensorMap map;
+  };
+  std::vector<UserMap> user_maps;
+  std::vector<std::unique_ptr<FinalArgs<kMaxFinal>>> fin;
 };
 
 }  // namespace
@@ -750,13 +759,14 @@ cudaLaunchConfig_t gemm_config(int lists, cudaStream_t s, cudaLaunchAttribute* a
   return cfg;
 }
 
-template <bool kGram, int kBN, int kStages>
-muon_status launch_gemm(muon_handle h, const GemmArgs& a, cudaStream_t s, int kind) {
+template <bool kGram, int kBN, int kStages, bool kFinal = false>
+muon_status launch_gemm(muon_handle h, const GemmArgs& a, const FinalArgs<kFinal ? kMaxFinal : 1>& f, cudaStream_t s,
+                        int kind) {
   if (a.num_tiles == 0) return MUON_OK;
   ProfScope ps(h, kind, s);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = gemm_config<kGram, kBN, kStages>(a.grid, s, attr);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kCluster>, a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kCluster, kFinal>, a, f);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(h, e, "tcgen05 GEMM launch");
@@ -764,34 +774,94 @@ muon_status launch_gemm(muon_handle h, const GemmArgs& a, cudaStream_t s, int ki
   return launch_checked(h, "tcgen05 GEMM kernel");
 }
 
+const FinalArgs<1> kNoFinal = {};
+
+// Fills the per-batch argument blocks that let the last combine write into the caller's
+// matrices `user` (update: W <- W - lr*s*X_k; else out <- X_k). Returns false, leaving the
+// separate update / copy kernel to do it, when a matrix is not bf16, not 16-byte aligned, its
+// ld is not a multiple of 8 elements, or a batch holds more than kMaxFinal matrices.
+bool prepare_final(muon_handle h, Plan& P, const muon_matrix* user, bool update, float lr) {
+  for (size_t j = 0; j < P.mats.size(); ++j) {
+    if (P.mats[j].skip) continue;
+    const muon_matrix& u = user[j];
+    if (u.dtype != MUON_BF16 || !aligned16(u.ptr) || u.ld % 8 != 0) return false;
+  }
+  if (P.fin.size() != P.batches.size()) {
+    P.fin.clear();
+    for (size_t b = 0; b < P.batches.size(); ++b) P.fin.push_back(std::make_unique<FinalArgs<kMaxFinal>>());
+  }
+  if (P.user_maps.size() != P.mats.size()) P.user_maps.assign(P.mats.size(), Plan::UserMap{});
+  for (size_t b = 0; b < P.batches.size(); ++b) {
+    FinalArgs<kMaxFinal>& F = *P.fin[b];
+    int running = 0;
+    for (int gi = 0; gi < P.batches[b].num_groups; ++gi) {
+      F.first[gi] = running;
+      running += P.groups[P.batches[b].first_group + gi].count;
+    }
+    if (running > kMaxFinal) return false;
+    F.update = update ? 1 : 0;
+  }
+  for (size_t j = 0; j < P.mats.size(); ++j) {
+    const MatInfo& mi = P.mats[j];
+    if (mi.skip) continue;
+    const muon_matrix& u = user[j];
+    Plan::UserMap& um = P.user_maps[j];
+    if (um.ptr != u.ptr || um.ld != u.ld) {
+      // 32 rows x 64 columns swizzled as the combine's tiles; transposed matrices take the
+      // transposed box, 64 rows x 32 columns, unswizzled.
+      const bool ok = mi.transposed
+                          ? encode_map(h, &um.map, u.ptr, mi.cols, mi.rows, 1, u.ld, 32, 64, false)
+                          : encode_map(h, &um.map, u.ptr, mi.cols, mi.rows, 1, u.ld, 64, 32, true);
+      if (!ok) {
+        um.ptr = nullptr;
+        return false;
+      }
+      um.ptr = u.ptr;
+      um.ld = u.ld;
+    }
+    FinalArgs<kMaxFinal>& F = *P.fin[mi.group / kMaxGroups];
+    const int slot = F.first[mi.group % kMaxGroups] + mi.idx;
+    F.map[slot] = um.map;
+    F.trans[slot] = mi.transposed ? 1 : 0;
+    const double sc = h->cfg.scale_lr_by_shape ? std::sqrt(std::max(1.0, double(mi.rows) / double(mi.cols))) : 1.0;
+    F.scale[slot] = update ? static_cast<float>(double(lr) * sc) : 0.f;
+  }
+  return true;
+}
+
 // k Newton-Schulz iterations on X0 (buffer 0). Returns the buffer holding X_k.
+// With `final_into_user`, the last combine writes into the caller's matrices (prepare_final).
 muon_status run_iterations(muon_handle h, const Plan& P, int steps, float a, float b, float c, cudaStream_t s,
-                           int* xk) {
+                           int* xk, bool final_into_user = false) {
   int t = 0;
   for (int it = 0; it < steps; ++it) {
-    for (const GemmBatch& B : P.batches) {
+    for (size_t bi = 0; bi < P.batches.size(); ++bi) {
+      const GemmBatch& B = P.batches[bi];
       muon_status st;
       if (c == 0.0f) {
         GemmArgs g = B.gram[t];
         g.s_acc = b;
         g.s_e = 0.f;
-        st = launch_gemm<true, kGramBN, kGramStages>(h, g, s, K_GRAM);
+        st = launch_gemm<true, kGramBN, kGramStages>(h, g, kNoFinal, s, K_GRAM);
       } else {
         GemmArgs g = B.gram_to_a[t];  // A = X X^T into the A buffer
         g.s_acc = 1.f;
         g.s_e = 0.f;
-        st = launch_gemm<true, kGramBN, kGramStages>(h, g, s, K_GRAM);
+        st = launch_gemm<true, kGramBN, kGramStages>(h, g, kNoFinal, s, K_GRAM);
         if (st != MUON_OK) return st;
         GemmArgs g2 = B.gram_aa;
         g2.s_acc = c;
         g2.s_e = b;
-        st = launch_gemm<true, kGramBN, kGramStages>(h, g2, s, K_GRAM_AA);
+        st = launch_gemm<true, kGramBN, kGramStages>(h, g2, kNoFinal, s, K_GRAM_AA);
       }
       if (st != MUON_OK) return st;
       GemmArgs cb = B.comb[t];
       cb.s_acc = 1.f;
       cb.s_e = a;
-      st = launch_gemm<false, kCombBN, kCombStages>(h, cb, s, K_COMBINE);
+      if (final_into_user && it == steps - 1)
+        st = launch_gemm<false, kCombBN, kCombStages, true>(h, cb, *P.fin[bi], s, K_COMBINE);
+      else
+        st = launch_gemm<false, kCombBN, kCombStages>(h, cb, kNoFinal, s, K_COMBINE);
       if (st != MUON_OK) return st;
     }
     t ^= 1;
@@ -1017,11 +1087,14 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
     cudaFree(h->err_dev);
     return MUON_ERR_CUDA;
   }
-  cudaError_t e1 = cudaFuncSetAttribute(ns_gemm_kernel<true, kGramBN, kGramStages, kCluster>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, GramShape::SMEM_BYTES);
-  cudaError_t e2 = cudaFuncSetAttribute(ns_gemm_kernel<false, kCombBN, kCombStages, kCluster>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, CombShape::SMEM_BYTES);
-  if (e1 != cudaSuccess || e2 != cudaSuccess) {
+  auto kgram = ns_gemm_kernel<true, kGramBN, kGramStages, kCluster, false>;
+  auto kcomb = ns_gemm_kernel<false, kCombBN, kCombStages, kCluster, false>;
+  auto kfinal = ns_gemm_kernel<false, kCombBN, kCombStages, kCluster, true>;
+  cudaError_t e1 = cudaFuncSetAttribute(kgram, cudaFuncAttributeMaxDynamicSharedMemorySize, GramShape::SMEM_BYTES);
+  cudaError_t e2 = cudaFuncSetAttribute(kcomb, cudaFuncAttributeMaxDynamicSharedMemorySize, CombShape::SMEM_BYTES);
+  cudaError_t e3 = cudaFuncSetAttribute(kfinal, cudaFuncAttributeMaxDynamicSharedMemorySize, CombShape::SMEM_BYTES);
+  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
+    cudaGetLastError();
     cudaFree(h->err_dev);
     return MUON_ERR_CUDA;
   }
@@ -1029,17 +1102,18 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
   h->max_lists = h->num_sms / kCluster;
   if (kCluster > 1) {
     cudaLaunchAttribute attr[2];
-    int n1 = 0, n2 = 0;
+    int n1 = 0, n2 = 0, n3 = 0;
     cudaLaunchConfig_t c1 = gemm_config<true, kGramBN, kGramStages>(1, nullptr, attr);
-    e1 = cudaOccupancyMaxActiveClusters(&n1, ns_gemm_kernel<true, kGramBN, kGramStages, kCluster>, &c1);
+    e1 = cudaOccupancyMaxActiveClusters(&n1, kgram, &c1);
     cudaLaunchConfig_t c2 = gemm_config<false, kCombBN, kCombStages>(1, nullptr, attr);
-    e2 = cudaOccupancyMaxActiveClusters(&n2, ns_gemm_kernel<false, kCombBN, kCombStages, kCluster>, &c2);
-    if (e1 != cudaSuccess || e2 != cudaSuccess || n1 < 1 || n2 < 1) {
+    e2 = cudaOccupancyMaxActiveClusters(&n2, kcomb, &c2);
+    e3 = cudaOccupancyMaxActiveClusters(&n3, kfinal, &c2);
+    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || n1 < 1 || n2 < 1 || n3 < 1) {
       cudaGetLastError();
       cudaFree(h->err_dev);
       return MUON_ERR_UNSUPPORTED;
     }
-    h->max_lists = std::min(n1, n2);
+    h->max_lists = std::min(n1, std::min(n2, n3));
   }
   *out = h.release();
   return MUON_OK;
@@ -1078,7 +1152,9 @@ muon_status muon_orthogonalize(muon_handle h, const muon_matrix* in, const muon_
   if ((st = launch_momentum<false>(h, *P, in, nullptr, 0.f, 0, s)) != MUON_OK) return st;
   if ((st = launch_map<kScale>(h, *P, in, 0, 0.f, true, s, K_SCALE)) != MUON_OK) return st;
   int xk = 0;
-  if ((st = run_iterations(h, *P, steps, a, b, c, s, &xk)) != MUON_OK) return st;
+  const bool direct = steps >= 1 && prepare_final(h, *P, out, false, 0.f);
+  if ((st = run_iterations(h, *P, steps, a, b, c, s, &xk, direct)) != MUON_OK) return st;
+  if (direct) return MUON_OK;
   return launch_map<kCopy>(h, *P, out, xk, 0.f, false, s, K_COPY);
 }
 
@@ -1097,7 +1173,11 @@ muon_status muon_step(muon_handle h, const muon_matrix* params, const muon_matri
   if ((st = launch_momentum<true>(h, *P, grads, momentum, beta, nesterov, s)) != MUON_OK) return st;
   if ((st = launch_map<kScale>(h, *P, nullptr, 0, 0.f, false, s, K_SCALE)) != MUON_OK) return st;
   int xk = 0;
-  if ((st = run_iterations(h, *P, h->cfg.steps, h->cfg.a, h->cfg.b, h->cfg.c, s, &xk)) != MUON_OK) return st;
+  // The update happens in the last combine's epilogue when the parameters allow it.
+  const bool direct = h->cfg.steps >= 1 && prepare_final(h, *P, params, true, lr);
+  if ((st = run_iterations(h, *P, h->cfg.steps, h->cfg.a, h->cfg.b, h->cfg.c, s, &xk, direct)) != MUON_OK)
+    return st;
+  if (direct) return MUON_OK;
   return launch_map<kUpdate>(h, *P, params, xk, lr, false, s, K_UPDATE);
 }
 

@@ -63,6 +63,23 @@ struct GemmArgs {
   int* err;
 };
 
+// The last combine of a call can write its result straight into the caller's
+// bf16 matrices: W <- W - scale * X_k (muon_step) or out <- X_k
+// (muon_orthogonalize). One tensor map per matrix, in the order
+// first[group] + matrix-within-group. trans = 1 when the caller's matrix is
+// X_k^T (rows > cols): its box is then 32 columns x 64 rows, unswizzled, and the
+// tile's values go in transposed.
+constexpr int kMaxFinal = 160;
+
+template <int N>
+struct FinalArgs {
+  CUtensorMap map[N];
+  float scale[N];
+  uint8_t trans[N];
+  int first[kMaxGroups];
+  int update;  // 1: W <- W - scale * X_k; 0: out <- X_k
+};
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -151,8 +168,9 @@ struct GemmShape {
 // half of B, and multicasts that half into both CTAs' shared memory. A stage
 // is refilled only when both CTAs' MMAs have released it, so every MMA commit
 // of a stage arrives on that stage's empty barrier in both CTAs.
-template <bool kGram, int kBN, int kStages, int kCluster>
-__global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs args) {
+template <bool kGram, int kBN, int kStages, int kCluster, bool kFinal>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    ns_gemm_kernel(const __grid_constant__ GemmArgs args, const __grid_constant__ FinalArgs<kFinal ? kMaxFinal : 1> fin) {
   using S = GemmShape<kGram, kBN, kStages>;
   constexpr int BM = S::BM, BK = S::BK;
   constexpr uint32_t A_BYTES = S::A_BYTES, B_BYTES = S::B_BYTES;
@@ -160,6 +178,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   constexpr uint16_t kPairMask = 0x3;
   static_assert(kBN == 256, "tile width");
   static_assert(kCluster == 1 || kCluster == 2, "cluster size");
+  static_assert(!(kGram && kFinal), "only the combine writes to the caller's matrices");
   static_assert(S::TMEM_COLS == 512, "TMEM allocation must be a power of two");
 
   extern __shared__ uint8_t smem_raw[];
@@ -205,7 +224,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     for (int g = 0; g < args.num_groups; ++g) {
       tma_prefetch_map(&args.map_a[g]);
       tma_prefetch_map(&args.map_b[g]);
-      tma_prefetch_map(&args.map_out[g]);
+      if (!kFinal) tma_prefetch_map(&args.map_out[g]);
       if (kGram) tma_prefetch_map(&args.map_mirror[g]);
       if (args.grp[g].e) tma_prefetch_map(&args.map_e[g]);
     }
@@ -412,6 +431,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           } else if (lane == 0) {
             bulk_wait_group_read0();  // the staging box is free once the previous store has read it
           }
+          const int x0 = col_base + box * 64;
+          if constexpr (kFinal) {
+            // Straight into the caller's matrix: the box at (x0, y0) of X_k, transposed for trans.
+            const int mi = fin.first[td.x] + td.y;
+            const bool tr = fin.trans[mi] != 0;
+            const int ux = tr ? y0 : x0, uy = tr ? x0 : y0;
+            if (fin.update) {
+              if (lane == 0) {
+                bulk_wait_group_read0();
+                mbar_arrive_expect_tx(ebar, 4096u);
+                tma_load_3d(stg_addr, &fin.map[mi], ebar, ux, uy, 0);
+              }
+              e_pending = true;
+              if (!mbar_wait_bounded(ebar, ephase, abort_flag, args.err)) {
+                ok = false;
+                break;
+              }
+              ephase ^= 1u;
+              e_pending = false;
+            } else if (lane == 0) {
+              bulk_wait_group_read0();
+            }
+            __syncwarp();
+            const float us = fin.scale[mi];
+            if (!tr) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t off = static_cast<uint32_t>(lane) * 128u + static_cast<uint32_t>((j ^ (lane & 7)) * 16);
+                uint4* p = reinterpret_cast<uint4*>(stg + off);
+                uint32_t ww[4] = {0u, 0u, 0u, 0u};
+                if (fin.update) {
+                  const uint4 w4 = *p;
+                  ww[0] = w4.x; ww[1] = w4.y; ww[2] = w4.z; ww[3] = w4.w;
+                }
+                uint32_t o[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                  const float lo = v[8 * j + 2 * h], hi = v[8 * j + 2 * h + 1];
+                  o[h] = fin.update ? pack_bf16x2(bf16_bits_to_float(ww[h] & 0xFFFFu) - us * lo,
+                                                  bf16_bits_to_float(ww[h] >> 16) - us * hi)
+                                    : pack_bf16x2(lo, hi);
+                }
+                *p = make_uint4(o[0], o[1], o[2], o[3]);
+              }
+            } else {
+              uint16_t* p = reinterpret_cast<uint16_t*>(stg);  // 64 rows x 32 columns
+#pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                const int idx = c * 32 + lane;
+                p[idx] = fin.update ? to_bf16_bits(bf16_bits_to_float(p[idx]) - us * v[c]) : to_bf16_bits(v[c]);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&fin.map[mi], stg_addr, ux, uy, 0);
+              bulk_commit_group();
+            }
+          } else {
           __syncwarp();
 #pragma unroll
           for (int k = 0; k < 32; ++k) packed[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
@@ -423,7 +501,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           }
           fence_proxy_async_smem();
           __syncwarp();
-          const int x0 = col_base + box * 64;
           if (lane == 0) {
             tma_store_3d(&args.map_out[td.x], stg_addr, x0, y0, td.y);
             bulk_commit_group();
@@ -443,6 +520,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
               tma_store_3d(&args.map_mirror[td.x], stg_addr, y0, x0, td.y);
               bulk_commit_group();
             }
+          }
           }
         }
       }

@@ -164,6 +164,32 @@ def test_step_bf16_params(muon):
         assert np.all(err <= bf16_ulp(w_new) + 0.05 * upd), (r, c, float(err.max()))
 
 
+@pytest.mark.parametrize("pad", [0, 3], ids=["direct", "fallback"])
+def test_step_bf16_params_ragged(muon, pad):
+    """Ragged and transposed bf16 params. pad = 0: the last combine writes W directly (16-byte rows);
+    pad = 3: ld is not a multiple of 8, so the separate update kernel runs. Both must agree with
+    the oracle to one bf16 ulp plus 5% of the largest update element."""
+    shapes = [(130, 70), (70, 130), (1, 5), (5, 1), (200, 64), (257, 129)]
+    w, g, m, p = step_case(shapes, "bf16", "bf16", seed=23)
+    lr = 0.02
+    bufs = [torch.zeros(r, c + pad, dtype=torch.bfloat16, device="cuda") for r, c in shapes]
+    P = [b[:, :c] for b, (r, c) in zip(bufs, shapes)]
+    for t, x in zip(P, p):
+        t.copy_(dev(x, "bf16"))
+    G = [dev(x, "bf16") for x in g]
+    M = [dev(x, "f32") for x in m]
+    muon.step(P, G, M, lr=lr, beta=0.95, nesterov=True)
+    torch.cuda.synchronize()
+    assert muon.get_error() == 0
+    for j, (r, c) in enumerate(shapes):
+        w_new, _, o = oracle.muon_step(p[j], g[j], m[j], lr, 0.95, True, 5, CUBIC)
+        upd = lr * oracle.lr_scale(r, c) * np.abs(o).max()
+        err = np.abs(host(P[j]) - w_new)
+        assert np.all(err <= bf16_ulp(w_new) + 0.05 * upd), (r, c, float(err.max()))
+        if pad:
+            assert torch.count_nonzero(bufs[j][:, c:]) == 0  # padding untouched
+
+
 def test_step_f32_grads_config1(muon):
     """One fp32 128x256 gradient N(0,1), zero momentum, beta 0.95, 5 cubic iterations."""
     w = wl.SINGLE_128x256
