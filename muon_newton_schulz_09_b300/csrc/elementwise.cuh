@@ -130,15 +130,20 @@ __device__ __forceinline__ float warp_sum(float s) {
 struct MomMat {
   const void* g;       // gradient or orthogonalize input (fp32 or bf16)
   float* buf;          // momentum, fp32
-  uint16_t* u;         // bf16 u, rows x cols contiguous
-  int64_t ld_g, ld_buf;
-  int rows, cols;
-  int vec_ok;          // contiguous (ld == cols), cols % 8 == 0 and 16-byte aligned: vector path
+  uint16_t* u;         // bf16 u in the Newton-Schulz orientation (n x m, ld_u), or nullptr (norm only)
+  int64_t ld_g, ld_buf, ld_u;
+  int rows, cols;      // caller orientation
+  int transposed;      // u = (g-side matrix)^T: written through a 128 x 64 shared-memory tile
+  int tiles_c;         // transposed: tiles along the caller's columns
+  int vec_ok;          // 16-byte vectors: flat path needs ld == cols everywhere and cols % 8 == 0;
+                       // transposed path needs every ld % 8 == 0; both need aligned pointers
   int block_begin;     // first block of this matrix in the launch
   int nchunks;         // blocks of this matrix = partial sums
   float* partial;      // nchunks partial sums of u^2
   int* ticket;         // arrivals; zero between calls (the last block resets it)
   float* inv;          // out: 1 / (||u||_F + eps)
+  float* post;         // out (or nullptr): scale the first Newton-Schulz products apply to u (1 when
+                       // the norm is outside the fold range and u was scaled in place instead)
 };
 
 struct MomArgs {
@@ -147,7 +152,21 @@ struct MomArgs {
   float beta;
   int nesterov;
   float eps;
+  int force_rescale;   // 1: every matrix takes the in-place scale (no folded scale)
 };
+
+// Norms for which the unscaled u can go through the fp32-accumulated Gram safely: every
+// element is below 1e10 (no overflow of its products) and typical elements are far above the
+// square root of the smallest normal float (no underflow). Outside it u is scaled first.
+constexpr float kFoldMinNorm = 1e-10f, kFoldMaxNorm = 1e10f;
+
+template <bool kStep, bool kSrcF32>
+__device__ __forceinline__ float momentum_u(float g, float& b, float beta, int nesterov) {
+  if (!kStep) return g;
+  const float nb = beta * b + g;
+  b = nb;
+  return nesterov ? g + beta * nb : nb;
+}
 
 template <bool kStep, bool kSrcF32>
 __global__ void __launch_bounds__(kEwThreads, kSrcF32 ? 3 : 4) momentum_norm_kernel(const __grid_constant__ MomArgs a) {
@@ -155,62 +174,124 @@ __global__ void __launch_bounds__(kEwThreads, kSrcF32 ? 3 : 4) momentum_norm_ker
   const int j = owner_of_block(a.m, a.count, static_cast<int>(blockIdx.x));
   const MomMat& M = a.m[j];
   const int chunk = static_cast<int>(blockIdx.x) - M.block_begin;
-  const int64_t cols = M.cols;
-  const int64_t n = static_cast<int64_t>(M.rows) * cols;
-  const int64_t e0 = static_cast<int64_t>(chunk) * kFlatChunk;
-  const int64_t e1 = min(n, e0 + kFlatChunk);
   const float beta = a.beta;
   float ss = 0.f;
 
-  if (M.vec_ok) {
-    // Vector path: contiguous rows (ld == cols), 16-byte aligned, so element e sits at offset e.
-    constexpr int V = kFlatChunk / (kEwThreads * 8);
-    Raw8<kSrcF32> gr[V];
-    Raw8<true> br[V];
+  if (!M.transposed) {
+    const int64_t cols = M.cols;
+    const int64_t n = static_cast<int64_t>(M.rows) * cols;
+    const int64_t e0 = static_cast<int64_t>(chunk) * kFlatChunk;
+    const int64_t e1 = min(n, e0 + kFlatChunk);
+    if (M.vec_ok) {
+      // Contiguous rows on every side (ld == cols), so element e sits at offset e.
+      constexpr int V = kFlatChunk / (kEwThreads * 8);
+      Raw8<kSrcF32> gr[V];
+      Raw8<true> br[V];
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      const int64_t e = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
-      if (e < e1) {
-        gr[v] = ld_raw8<kSrcF32>(M.g, e);
-        if (kStep) br[v] = ld_raw8<true>(M.buf, e);
+      for (int v = 0; v < V; ++v) {
+        const int64_t e = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
+        if (e < e1) {
+          gr[v] = ld_raw8<kSrcF32>(M.g, e);
+          if (kStep) br[v] = ld_raw8<true>(M.buf, e);
+        }
       }
-    }
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      const int64_t e = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
-      if (e < e1) {
-        float g[8], b[8], u[8];
-        unpack8<kSrcF32>(gr[v], g);
-        if (kStep) unpack8<true>(br[v], b);
+      for (int v = 0; v < V; ++v) {
+        const int64_t e = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
+        if (e < e1) {
+          float g[8], b[8], u[8];
+          unpack8<kSrcF32>(gr[v], g);
+          if (kStep) unpack8<true>(br[v], b);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (kStep) {
-            const float nb = beta * b[k] + g[k];
-            b[k] = nb;
-            u[k] = a.nesterov ? g[k] + beta * nb : nb;
-          } else {
-            u[k] = g[k];
+          for (int k = 0; k < 8; ++k) {
+            u[k] = momentum_u<kStep, kSrcF32>(g[k], b[k], beta, a.nesterov);
+            ss += u[k] * u[k];
           }
-          ss += u[k] * u[k];
+          if (kStep) store8<true>(M.buf, e, b);
+          if (M.u) store8<false>(M.u, e, u);
         }
-        if (kStep) {
-          store8<true>(M.buf, e, b);
-          store8<false>(M.u, e, u);
-        }
+      }
+    } else {
+      for (int64_t e = e0 + threadIdx.x; e < e1; e += kEwThreads) {
+        const int64_t row = e / cols, col = e - row * cols;
+        const float g = load1<kSrcF32>(M.g, row * M.ld_g + col);
+        float b = kStep ? M.buf[row * M.ld_buf + col] : 0.f;
+        const float u = momentum_u<kStep, kSrcF32>(g, b, beta, a.nesterov);
+        if (kStep) M.buf[row * M.ld_buf + col] = b;
+        if (M.u) M.u[row * M.ld_u + col] = f_to_bf16(u);
+        ss += u * u;
       }
     }
   } else {
-    for (int64_t e = e0 + threadIdx.x; e < e1; e += kEwThreads) {
-      const int64_t row = e / cols, col = e - row * cols;
-      const float g = load1<kSrcF32>(M.g, row * M.ld_g + col);
-      float u = g;
-      if (kStep) {
-        const float nb = beta * M.buf[row * M.ld_buf + col] + g;
-        M.buf[row * M.ld_buf + col] = nb;
-        u = a.nesterov ? g + beta * nb : nb;
-        M.u[e] = f_to_bf16(u);
+    // Caller tile rows r0..r0+127, columns c0..c0+63; u^T rows c0..c0+63, columns r0..r0+127.
+    __shared__ float tile[128][kTile + 1];
+    const int r0 = (chunk / M.tiles_c) * 128;
+    const int c0 = (chunk % M.tiles_c) * kTile;
+    const int sub = threadIdx.x >> 3;
+    const int c8 = (threadIdx.x & 7) * 8;
+    constexpr int P1 = 128 / 32;
+    Raw8<kSrcF32> gr[P1];
+    Raw8<true> br[P1];
+#pragma unroll
+    for (int p = 0; p < P1; ++p) {
+      const int gr_ = r0 + p * 32 + sub, gc = c0 + c8;
+      if (M.vec_ok && gr_ < M.rows && gc + 7 < M.cols) {
+        gr[p] = ld_raw8<kSrcF32>(M.g, static_cast<int64_t>(gr_) * M.ld_g + gc);
+        if (kStep) br[p] = ld_raw8<true>(M.buf, static_cast<int64_t>(gr_) * M.ld_buf + gc);
       }
-      ss += u * u;
+    }
+#pragma unroll
+    for (int p = 0; p < P1; ++p) {
+      const int r = p * 32 + sub;
+      const int row = r0 + r, gc = c0 + c8;
+      float u[8];
+      if (M.vec_ok && row < M.rows && gc + 7 < M.cols) {
+        float g[8], b[8];
+        unpack8<kSrcF32>(gr[p], g);
+        if (kStep) unpack8<true>(br[p], b);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) u[k] = momentum_u<kStep, kSrcF32>(g[k], b[k], beta, a.nesterov);
+        if (kStep) store8<true>(M.buf, static_cast<int64_t>(row) * M.ld_buf + gc, b);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          u[k] = 0.f;
+          if (row < M.rows && gc + k < M.cols) {
+            const float g = load1<kSrcF32>(M.g, static_cast<int64_t>(row) * M.ld_g + gc + k);
+            float b = kStep ? M.buf[static_cast<int64_t>(row) * M.ld_buf + gc + k] : 0.f;
+            u[k] = momentum_u<kStep, kSrcF32>(g, b, beta, a.nesterov);
+            if (kStep) M.buf[static_cast<int64_t>(row) * M.ld_buf + gc + k] = b;
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        ss += u[k] * u[k];
+        tile[r][c8 + k] = u[k];
+      }
+    }
+    if (M.u) {
+      __syncthreads();
+      // 16 threads per u^T row (128 columns), 16 rows per pass.
+      const int drow = threadIdx.x >> 4;
+      const int dcol = (threadIdx.x & 15) * 8;
+#pragma unroll
+      for (int p = 0; p < kTile / 16; ++p) {
+        const int cc = p * 16 + drow;
+        const int dr = c0 + cc, dc = r0 + dcol;
+        if (dr >= M.cols) continue;
+        float uv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) uv[k] = tile[dcol + k][cc];
+        const int64_t di = static_cast<int64_t>(dr) * M.ld_u + dc;
+        if (M.vec_ok && dc + 7 < M.rows) {
+          store8<false>(M.u, di, uv);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (dc + k < M.rows) M.u[di + k] = f_to_bf16(uv[k]);
+        }
+      }
     }
   }
 
@@ -240,12 +321,32 @@ __global__ void __launch_bounds__(kEwThreads, kSrcF32 ? 3 : 4) momentum_norm_ker
     __syncthreads();
     if (lane == 0) wsum[warp] = s;
     __syncthreads();
+    __shared__ float inv_s;
+    __shared__ int fold_s;
     if (threadIdx.x == 0) {
       float tot = 0.f;
 #pragma unroll
       for (int w = 0; w < kEwThreads / 32; ++w) tot += wsum[w];
-      *M.inv = 1.0f / (sqrtf(tot) + a.eps);
+      const float norm = sqrtf(tot);
+      const float inv = 1.0f / (norm + a.eps);
+      *M.inv = inv;
+      const bool fold = !a.force_rescale && norm >= kFoldMinNorm && norm <= kFoldMaxNorm;
+      if (M.post) *M.post = fold ? inv : 1.0f;
+      inv_s = inv;
+      fold_s = fold ? 1 : 0;
       *M.ticket = 0;
+    }
+    __syncthreads();
+    if (M.u && !fold_s) {
+      // Norm outside the fold range: this block scales the whole of u in place (rare; every other
+      // block's u is visible after its fence and ticket).
+      const float f = inv_s;
+      const int64_t n = M.transposed ? M.cols : M.rows, m = M.transposed ? M.rows : M.cols;
+      for (int64_t e = threadIdx.x; e < n * m; e += kEwThreads) {
+        const int64_t row = e / m, col = e - row * m;
+        uint16_t* p = M.u + row * M.ld_u + col;
+        *p = f_to_bf16(bf16_to_f(__ldcg(p)) * f);
+      }
     }
   }
 }

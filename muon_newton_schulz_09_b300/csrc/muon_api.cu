@@ -128,13 +128,15 @@ struct MatInfo {
   bool transposed = false;
   int group = -1, idx = -1;  // shape group and position within it
   int64_t n = 0, m = 0;      // oriented shape
-  int64_t nchunks = 0;       // norm partials
+  int64_t nchunks = 0;       // norm partials: blocks of the flat or the transposed-tile decomposition
   int64_t partial_off = 0;
+  int gslot = -1;            // index in group order (group's first slot + idx)
 };
 
 struct Group {
   int64_t n = 0, m = 0;
   int count = 0;
+  int first_slot = 0;  // the group's first matrix in group order
   int64_t ld_x = 0, ld_p = 0;
   size_t x_off[2] = {0, 0}, p_off = 0, a_off = 0;  // byte offsets in the workspace
 };
@@ -163,6 +165,7 @@ struct Plan {
   float* partial = nullptr;
   int* tickets = nullptr;
   float* inv = nullptr;
+  float* post = nullptr;   // group order: scale folded into the first iteration's products
   int4* tiles_dev = nullptr;
   int* begin_dev = nullptr;
   uint64_t last_use = 0;
@@ -300,8 +303,15 @@ void group_shapes(const std::vector<std::pair<int64_t, int64_t>>& shapes, std::v
     }
     mi.group = it->second;
     mi.idx = groups[mi.group].count++;
-    mi.nchunks = ceil_div(mi.rows * mi.cols, kFlatChunk);
+    mi.nchunks = std::max(ceil_div(mi.rows * mi.cols, kFlatChunk), ceil_div(mi.rows, 128) * ceil_div(mi.cols, kTile));
   }
+  int slot = 0;
+  for (Group& g : groups) {
+    g.first_slot = slot;
+    slot += g.count;
+  }
+  for (MatInfo& mi : mats)
+    if (!mi.skip) mi.gslot = groups[mi.group].first_slot + mi.idx;
 }
 
 // One GEMM launch's schedule: tiles grouped by CTA, and CTA b's range
@@ -400,6 +410,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
   const size_t part_off = take(static_cast<size_t>(std::max<int64_t>(nparts, 1)) * 4);
   const size_t tick_off = take(P.mats.size() * 4 + 4);
   const size_t inv_off = take(P.mats.size() * 4 + 4);
+  const size_t post_off = take(P.mats.size() * 4 + 4);
   P.ws_bytes = off;
 
   cudaError_t e = cudaMalloc(&P.ws, P.ws_bytes);
@@ -410,6 +421,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
   P.partial = reinterpret_cast<float*>(P.ws + part_off);
   P.tickets = reinterpret_cast<int*>(P.ws + tick_off);
   P.inv = reinterpret_cast<float*>(P.ws + inv_off);
+  P.post = reinterpret_cast<float*>(P.ws + post_off);
   e = cudaMemset(P.ws, 0, P.ws_bytes);
   if (e != cudaSuccess) {
     free_plan(&P);
@@ -497,7 +509,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
         B.gram[t].map_b[gi] = B.gram[t].map_a[gi];
         ok &= encode_map(h, &B.gram[t].map_out[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 32);
         ok &= encode_map(h, &B.gram[t].map_mirror[gi], pbuf, g.n, g.n, g.count, g.ld_p, 32, 64, false);
-        B.gram[t].grp[gi] = GemmGroup{nullptr, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
+        B.gram[t].grp[gi] = GemmGroup{nullptr, nullptr, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
                                       static_cast<int>(g.ld_p), static_cast<int>(ceil_div(g.m, 64))};
         // The same Gram writing A = X X^T into the A buffer (first pass when c != 0).
         B.gram_to_a[t].map_a[gi] = B.gram[t].map_a[gi];
@@ -510,7 +522,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
         ok &= encode_map(h, &B.comb[t].map_b[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 64);
         ok &= encode_map(h, &B.comb[t].map_out[gi], xb[1 - t], g.m, g.n, g.count, g.ld_x, 64, 32);
         ok &= encode_map(h, &B.comb[t].map_e[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 32);
-        B.comb[t].grp[gi] = GemmGroup{reinterpret_cast<uint16_t*>(xb[t]), g.n * g.ld_x, static_cast<int>(g.n),
+        B.comb[t].grp[gi] = GemmGroup{reinterpret_cast<uint16_t*>(xb[t]), nullptr, g.n * g.ld_x, static_cast<int>(g.n),
                                       static_cast<int>(g.m), static_cast<int>(g.ld_x),
                                       static_cast<int>(ceil_div(g.n, 64))};
       }
@@ -520,7 +532,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
       ok &= encode_map(h, &B.gram_aa.map_out[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 32);
       ok &= encode_map(h, &B.gram_aa.map_mirror[gi], pbuf, g.n, g.n, g.count, g.ld_p, 32, 64, false);
       ok &= encode_map(h, &B.gram_aa.map_e[gi], abuf, g.n, g.n, g.count, g.ld_p, 64, 32);
-      B.gram_aa.grp[gi] = GemmGroup{abuf, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
+      B.gram_aa.grp[gi] = GemmGroup{abuf, nullptr, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
                                     static_cast<int>(g.ld_p), static_cast<int>(ceil_div(g.n, 64))};
       if (!ok) {
         free_plan(&P);
@@ -596,9 +608,12 @@ muon_status launch_checked(muon_handle h, const char* what) {
 }
 
 // Norm pass (kStep = false: u = input) or momentum + norm (kStep = true).
+// Norm pass (kStep = false: u = input, nothing written) or momentum + norm (kStep = true:
+// u written in the Newton-Schulz orientation into the first X buffer, unscaled; the scale is
+// folded into the first iteration, or applied in place by the kernel for norms outside the fold range).
 template <bool kStep>
 muon_status launch_momentum(muon_handle h, const Plan& P, const muon_matrix* src, const muon_matrix* buf, float beta,
-                            int nesterov, cudaStream_t s) {
+                            int nesterov, int force_rescale, cudaStream_t s) {
   const bool f32 = [&] {
     for (size_t j = 0; j < P.mats.size(); ++j)
       if (!P.mats[j].skip) return src[j].dtype == MUON_F32;
@@ -609,6 +624,7 @@ muon_status launch_momentum(muon_handle h, const Plan& P, const muon_matrix* src
   a.beta = beta;
   a.nesterov = nesterov ? 1 : 0;
   a.eps = h->cfg.eps;
+  a.force_rescale = force_rescale;
   int blocks = 0;
   auto flush = [&]() -> muon_status {
     if (a.count == 0) return MUON_OK;
@@ -624,23 +640,36 @@ muon_status launch_momentum(muon_handle h, const Plan& P, const muon_matrix* src
   for (size_t j = 0; j < P.mats.size(); ++j) {
     const MatInfo& mi = P.mats[j];
     if (mi.skip) continue;
+    const Group& g = P.groups[mi.group];
     MomMat& M = a.m[a.count];
     M.g = src[j].ptr;
     M.ld_g = src[j].ld;
     M.buf = kStep ? static_cast<float*>(buf[j].ptr) : nullptr;
     M.ld_buf = kStep ? buf[j].ld : 0;
-    M.u = kStep ? x_slot(P, mi, 1) : nullptr;  // u lives in the second X buffer until the scale pass reads it
+    M.u = kStep ? x_slot(P, mi, 0) : nullptr;
+    M.ld_u = g.ld_x;
     M.rows = static_cast<int>(mi.rows);
     M.cols = static_cast<int>(mi.cols);
-    bool vec = (mi.cols % 8 == 0) && (src[j].ld == mi.cols) && aligned16(src[j].ptr);
-    if (kStep) vec = vec && (buf[j].ld == mi.cols) && aligned16(buf[j].ptr);
+    M.transposed = (kStep && mi.transposed) ? 1 : 0;
+    bool vec = aligned16(src[j].ptr) && (!kStep || aligned16(buf[j].ptr));
+    int nblk;
+    if (M.transposed) {
+      vec = vec && src[j].ld % 8 == 0 && buf[j].ld % 8 == 0;
+      M.tiles_c = static_cast<int>(ceil_div(mi.cols, kTile));
+      nblk = static_cast<int>(ceil_div(mi.rows, 128) * M.tiles_c);
+    } else {
+      vec = vec && mi.cols % 8 == 0 && src[j].ld == mi.cols && (!kStep || (buf[j].ld == mi.cols && g.ld_x == mi.cols));
+      M.tiles_c = 0;
+      nblk = static_cast<int>(ceil_div(mi.rows * mi.cols, kFlatChunk));
+    }
     M.vec_ok = vec ? 1 : 0;
     M.block_begin = blocks;
-    M.nchunks = static_cast<int>(mi.nchunks);
+    M.nchunks = nblk;
     M.partial = P.partial + mi.partial_off;
     M.ticket = P.tickets + j;
     M.inv = P.inv + j;
-    blocks += M.nchunks;
+    M.post = kStep ? P.post + mi.gslot : nullptr;
+    blocks += nblk;
     if (++a.count == kEwMax) {
       muon_status st = flush();
       if (st != MUON_OK) return st;
@@ -665,10 +694,10 @@ muon_status launch_map_dispatch(muon_handle h, const MapArgs& a, int blocks, boo
   return launch_checked(h, "map kernel");
 }
 
-// kMode = kScale: src = u (step) or input (orthogonalize) in the caller's orientation, dst = X0 slot.
+// kMode = kScale: src = the caller's input (orthogonalize), dst = X0 slot, oriented.
 // kMode = kUpdate / kCopy: src = X_k slot (oriented), dst = params / out in the caller's orientation.
 template <int kMode>
-muon_status launch_map(muon_handle h, const Plan& P, const muon_matrix* user, int xk, float lr, bool scale_mode_user,
+muon_status launch_map(muon_handle h, const Plan& P, const muon_matrix* user, int xk, float lr,
                        cudaStream_t s, int kind) {
   bool user_f32 = false;
   for (size_t j = 0; user && j < P.mats.size(); ++j)
@@ -694,15 +723,9 @@ muon_status launch_map(muon_handle h, const Plan& P, const muon_matrix* user, in
     MapMat& M = a.m[a.count];
     M.transposed = mi.transposed ? 1 : 0;
     if (kMode == kScale) {
-      if (scale_mode_user) {  // orthogonalize: the caller's input
-        M.src = user[j].ptr;
-        M.ld_src = user[j].ld;
-        src_f32 = user_f32;
-      } else {  // step: u, bf16, rows x cols contiguous in the second X buffer
-        M.src = x_slot(P, mi, 1);
-        M.ld_src = mi.cols;
-        src_f32 = false;
-      }
+      M.src = user[j].ptr;  // the caller's input (muon_orthogonalize)
+      M.ld_src = user[j].ld;
+      src_f32 = user_f32;
       M.dst = x_slot(P, mi, 0);
       M.ld_dst = g.ld_x;
       M.sr = static_cast<int>(mi.rows);
@@ -831,20 +854,29 @@ bool prepare_final(muon_handle h, Plan& P, const muon_matrix* user, bool update,
 
 // k Newton-Schulz iterations on X0 (buffer 0). Returns the buffer holding X_k.
 // With `final_into_user`, the last combine writes into the caller's matrices (prepare_final).
+// With `folded_scale`, X0 holds u unscaled and the first iteration's Gram and combine apply
+// the per-matrix scale (P.post).
 muon_status run_iterations(muon_handle h, const Plan& P, int steps, float a, float b, float c, cudaStream_t s,
-                           int* xk, bool final_into_user = false) {
+                           int* xk, bool final_into_user = false, bool folded_scale = false) {
   int t = 0;
   for (int it = 0; it < steps; ++it) {
     for (size_t bi = 0; bi < P.batches.size(); ++bi) {
       const GemmBatch& B = P.batches[bi];
       muon_status st;
+      const bool first = folded_scale && it == 0;
+      auto with_post = [&](GemmArgs& ga) {
+        if (!first) return;
+        for (int gi = 0; gi < ga.num_groups; ++gi) ga.grp[gi].post = P.post + P.groups[B.first_group + gi].first_slot;
+      };
       if (c == 0.0f) {
         GemmArgs g = B.gram[t];
+        with_post(g);
         g.s_acc = b;
         g.s_e = 0.f;
         st = launch_gemm<true, kGramBN, kGramStages>(h, g, kNoFinal, s, K_GRAM);
       } else {
         GemmArgs g = B.gram_to_a[t];  // A = X X^T into the A buffer
+        with_post(g);
         g.s_acc = 1.f;
         g.s_e = 0.f;
         st = launch_gemm<true, kGramBN, kGramStages>(h, g, kNoFinal, s, K_GRAM);
@@ -856,6 +888,7 @@ muon_status run_iterations(muon_handle h, const Plan& P, int steps, float a, flo
       }
       if (st != MUON_OK) return st;
       GemmArgs cb = B.comb[t];
+      with_post(cb);
       cb.s_acc = 1.f;
       cb.s_e = a;
       if (final_into_user && it == steps - 1)
@@ -1149,13 +1182,13 @@ muon_status muon_orthogonalize(muon_handle h, const muon_matrix* in, const muon_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Plan* P = nullptr;
   if ((st = get_plan(h, shape_key(in, count), &P)) != MUON_OK) return st;
-  if ((st = launch_momentum<false>(h, *P, in, nullptr, 0.f, 0, s)) != MUON_OK) return st;
-  if ((st = launch_map<kScale>(h, *P, in, 0, 0.f, true, s, K_SCALE)) != MUON_OK) return st;
+  if ((st = launch_momentum<false>(h, *P, in, nullptr, 0.f, 0, 0, s)) != MUON_OK) return st;
+  if ((st = launch_map<kScale>(h, *P, in, 0, 0.f, s, K_SCALE)) != MUON_OK) return st;
   int xk = 0;
   const bool direct = steps >= 1 && prepare_final(h, *P, out, false, 0.f);
   if ((st = run_iterations(h, *P, steps, a, b, c, s, &xk, direct)) != MUON_OK) return st;
   if (direct) return MUON_OK;
-  return launch_map<kCopy>(h, *P, out, xk, 0.f, false, s, K_COPY);
+  return launch_map<kCopy>(h, *P, out, xk, 0.f, s, K_COPY);
 }
 
 muon_status muon_step(muon_handle h, const muon_matrix* params, const muon_matrix* grads, const muon_matrix* momentum,
@@ -1170,15 +1203,19 @@ muon_status muon_step(muon_handle h, const muon_matrix* params, const muon_matri
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Plan* P = nullptr;
   if ((st = get_plan(h, shape_key(params, count), &P)) != MUON_OK) return st;
-  if ((st = launch_momentum<true>(h, *P, grads, momentum, beta, nesterov, s)) != MUON_OK) return st;
-  if ((st = launch_map<kScale>(h, *P, nullptr, 0, 0.f, false, s, K_SCALE)) != MUON_OK) return st;
+  // u goes into the first X buffer unscaled; its 1/(||u||_F + eps) is folded into the first
+  // iteration's Gram and combine, except for norms outside the safe range, where the momentum
+  // kernel scales u in place (and always with zero iterations).
+  const int steps = h->cfg.steps;
+  if ((st = launch_momentum<true>(h, *P, grads, momentum, beta, nesterov, steps == 0 ? 1 : 0, s)) != MUON_OK)
+    return st;
   int xk = 0;
   // The update happens in the last combine's epilogue when the parameters allow it.
-  const bool direct = h->cfg.steps >= 1 && prepare_final(h, *P, params, true, lr);
-  if ((st = run_iterations(h, *P, h->cfg.steps, h->cfg.a, h->cfg.b, h->cfg.c, s, &xk, direct)) != MUON_OK)
+  const bool direct = steps >= 1 && prepare_final(h, *P, params, true, lr);
+  if ((st = run_iterations(h, *P, steps, h->cfg.a, h->cfg.b, h->cfg.c, s, &xk, direct, true)) != MUON_OK)
     return st;
   if (direct) return MUON_OK;
-  return launch_map<kUpdate>(h, *P, params, xk, lr, false, s, K_UPDATE);
+  return launch_map<kUpdate>(h, *P, params, xk, lr, s, K_UPDATE);
 }
 
 muon_status muon_get_error(muon_handle h, void* stream) {

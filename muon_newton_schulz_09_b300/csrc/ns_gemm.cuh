@@ -41,6 +41,8 @@ constexpr int kEpilogueThreads = 256;
 
 struct GemmGroup {
   const uint16_t* e;      // non-null when the epilogue adds s_e * E (E read through map_e)
+  const float* post;      // per-matrix scale of this launch's operand X (nullptr: 1); the Gram
+                          // output takes post^2, the combine output post (X0 left unscaled)
   int64_t mat_stride;     // elements between consecutive matrices of e
   int rows_out, cols_out, ld_out;
   int nk;                 // number of 64-wide k-blocks of the contraction
@@ -381,6 +383,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool mirror = kGram && (block_col > I);
       const int col_base = td.w * kBN + half * kHalfCols;
       const int y0 = I * BM + quarter * 32;
+      // X = post * X' with X' the stored operand: the Gram gets post^2 on the product, the
+      // combine post on both of its terms.
+      const float post = G.post ? __ldg(G.post + td.y) : 1.0f;
+      const float s_acc = args.s_acc * (kGram ? post * post : post);
+      const float s_e = args.s_e * (kGram ? 1.0f : post);
       // E box `box` into the staging buffer, once the last store from it has been read.
       auto load_addend = [&](int box) {
         if (lane == 0) {
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tmem_base + lane_field + static_cast<uint32_t>(acc * kBN + half * kHalfCols + box * 64 + cc * 32), r);
             tmem_load_wait();
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[cc * 32 + k] = args.s_acc * __uint_as_float(r[k]);
+            for (int k = 0; k < 32; ++k) v[cc * 32 + k] = s_acc * __uint_as_float(r[k]);
           }
           if (has_e) {
             if (!mbar_wait_bounded(ebar, ephase, abort_flag, args.err)) {
@@ -424,8 +431,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
               for (int h = 0; h < 4; ++h) {
-                v[8 * j + 2 * h] += args.s_e * bf16_bits_to_float(ww[h] & 0xFFFFu);
-                v[8 * j + 2 * h + 1] += args.s_e * bf16_bits_to_float(ww[h] >> 16);
+                v[8 * j + 2 * h] += s_e * bf16_bits_to_float(ww[h] & 0xFFFFu);
+                v[8 * j + 2 * h + 1] += s_e * bf16_bits_to_float(ww[h] >> 16);
               }
             }
           } else if (lane == 0) {

@@ -190,6 +190,42 @@ def test_step_bf16_params_ragged(muon, pad):
             assert torch.count_nonzero(bufs[j][:, c:]) == 0  # padding untouched
 
 
+@pytest.mark.parametrize("scale", [1e-13, 1e12], ids=["tiny", "huge"])
+def test_step_extreme_gradient_scale(muon, scale):
+    """Gradient norms outside [1e-10, 1e10]: u is scaled in place before the first products instead of
+    through them, and O is the same as for a gradient of ordinary size (Newton-Schulz is scale invariant)."""
+    shapes = [(256, 512), (512, 256), (130, 70)]
+    w, g, _, _ = step_case(shapes, "bf16", "f32", seed=24)
+    gs = [wl.bf16_round((x.astype(np.float64) * scale).astype(np.float32)) for x in g]
+    lr = 0.02
+    P = [torch.zeros(sh, device="cuda") for sh in shapes]
+    M = [torch.zeros(sh, device="cuda") for sh in shapes]
+    muon.step(P, [dev(x, "bf16") for x in gs], M, lr=lr, beta=0.95, nesterov=True)
+    torch.cuda.synchronize()
+    assert muon.get_error() == 0
+    for j, (r, c) in enumerate(shapes):
+        _, _, o = oracle.muon_step(np.zeros((r, c)), gs[j], np.zeros((r, c)), lr, 0.95, True, 5, CUBIC)
+        got = -host(P[j]) / (lr * oracle.lr_scale(r, c))
+        assert np.isfinite(got).all()
+        assert rel_f(got, o) < TOL, (r, c, rel_f(got, o))
+
+
+def test_step_zero_iterations_is_normalised_momentum():
+    """steps = 0: O is X0 = u / (||u||_F + eps) itself, in the caller's orientation."""
+    from muon_newton_schulz_09_b300 import Muon
+    shapes = [(192, 320), (320, 192)]
+    w, g, m, _ = step_case(shapes, "bf16", "f32", seed=25)
+    P = [torch.zeros(sh, device="cuda") for sh in shapes]
+    with Muon(0, steps=0) as m0:
+        m0.step(P, [dev(x, "bf16") for x in g], [dev(x, "f32") for x in m], lr=1.0, beta=0.9, nesterov=False)
+        torch.cuda.synchronize()
+        assert m0.get_error() == 0
+    for j, (r, c) in enumerate(shapes):
+        _, u = oracle.momentum(g[j], m[j], 0.9, False)
+        want = oracle.frobenius_normalize(u)
+        assert rel_f(-host(P[j]) / oracle.lr_scale(r, c), want) < 4e-3
+
+
 def test_step_f32_grads_config1(muon):
     """One fp32 128x256 gradient N(0,1), zero momentum, beta 0.95, 5 cubic iterations."""
     w = wl.SINGLE_128x256
