@@ -32,14 +32,16 @@ using namespace muon;
 
 namespace {
 
-constexpr int kGramBN = 256, kGramStages = 4;
-constexpr int kCombBN = 256, kCombStages = 4;
-#ifndef MUON_GEMM_CLUSTER
-#define MUON_GEMM_CLUSTER 2
+#ifndef MUON_GEMM_PAIR
+#define MUON_GEMM_PAIR 1
 #endif
-constexpr int kCluster = MUON_GEMM_CLUSTER;  // CTAs sharing one B block through TMA multicast
-using GramShape = GemmShape<true, kGramBN, kGramStages>;
-using CombShape = GemmShape<false, kCombBN, kCombStages>;
+// Paired-SM MMAs (tcgen05 cta_group::2): each CTA holds half of B, so a stage is 32 KB and six fit.
+constexpr bool kPairMma = MUON_GEMM_PAIR != 0;
+constexpr int kGramBN = 256, kGramStages = kPairMma ? 6 : 4;
+constexpr int kCombBN = 256, kCombStages = kPairMma ? 6 : 4;
+constexpr int kCluster = 2;  // the two CTAs that share one B block
+using GramShape = GemmShape<true, kGramBN, kGramStages, kPairMma>;
+using CombShape = GemmShape<false, kCombBN, kCombStages, kPairMma>;
 
 constexpr int64_t kMaxDim = 1 << 20;          // rows or cols
 constexpr int64_t kMaxShort = 32768;          // min(rows, cols): the n x n Gram lives in workspace
@@ -769,7 +771,7 @@ cudaLaunchConfig_t gemm_config(int lists, cudaStream_t s, cudaLaunchAttribute* a
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(lists * kCluster), 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = GemmShape<kGram, kBN, kStages>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = GemmShape<kGram, kBN, kStages, kPairMma>::SMEM_BYTES;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCluster;
@@ -789,7 +791,7 @@ muon_status launch_gemm(muon_handle h, const GemmArgs& a, const FinalArgs<kFinal
   ProfScope ps(h, kind, s);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = gemm_config<kGram, kBN, kStages>(a.grid, s, attr);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kCluster, kFinal>, a, f);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kCluster, kFinal, kPairMma>, a, f);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(h, e, "tcgen05 GEMM launch");
@@ -1120,9 +1122,9 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
     cudaFree(h->err_dev);
     return MUON_ERR_CUDA;
   }
-  auto kgram = ns_gemm_kernel<true, kGramBN, kGramStages, kCluster, false>;
-  auto kcomb = ns_gemm_kernel<false, kCombBN, kCombStages, kCluster, false>;
-  auto kfinal = ns_gemm_kernel<false, kCombBN, kCombStages, kCluster, true>;
+  auto kgram = ns_gemm_kernel<true, kGramBN, kGramStages, kCluster, false, kPairMma>;
+  auto kcomb = ns_gemm_kernel<false, kCombBN, kCombStages, kCluster, false, kPairMma>;
+  auto kfinal = ns_gemm_kernel<false, kCombBN, kCombStages, kCluster, true, kPairMma>;
   cudaError_t e1 = cudaFuncSetAttribute(kgram, cudaFuncAttributeMaxDynamicSharedMemorySize, GramShape::SMEM_BYTES);
   cudaError_t e2 = cudaFuncSetAttribute(kcomb, cudaFuncAttributeMaxDynamicSharedMemorySize, CombShape::SMEM_BYTES);
   cudaError_t e3 = cudaFuncSetAttribute(kfinal, cudaFuncAttributeMaxDynamicSharedMemorySize, CombShape::SMEM_BYTES);

@@ -152,12 +152,13 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <bool kGram, int kBN, int kStages>
+template <bool kGram, int kBN, int kStages, bool kPair = false>
 struct GemmShape {
   static constexpr int BM = 128;
   static constexpr int BK = 64;
   static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = kBN * BK * 2;
+  // Paired-SM MMAs: each CTA holds only its half of B's columns.
+  static constexpr uint32_t B_BYTES = (kPair ? kBN / 2 : kBN) * BK * 2;
   static constexpr uint32_t TMEM_COLS = 2 * kBN;
   static constexpr uint32_t STAGING_BYTES = 8 * 4096;  // one 32 x 64 bf16 box per epilogue warp
   static constexpr uint32_t BAR_BYTES = 8 * (2 * kStages + 5 + 8) + 16;  // + one addend barrier per epilogue warp
@@ -165,19 +166,29 @@ struct GemmShape {
   static constexpr uint32_t SMEM_BYTES = 1024 + kStages * (A_BYTES + B_BYTES) + STAGING_BYTES + BAR_BYTES;
 };
 
-// kCluster = 2: the two CTAs of a cluster take tile rows I and I+1 of the same
-// tile column, so they need the same B block. Each loads its own A and one
-// half of B, and multicasts that half into both CTAs' shared memory. A stage
-// is refilled only when both CTAs' MMAs have released it, so every MMA commit
-// of a stage arrives on that stage's empty barrier in both CTAs.
-template <bool kGram, int kBN, int kStages, int kCluster, bool kFinal>
+// The two CTAs of a cluster take tile rows I and I+1 of the same tile column,
+// so they need the same B block.
+//
+// kPair = false (1-SM MMAs, M = 128): each CTA loads its own A and one half of
+// B, and multicasts that half into both CTAs' shared memory. A stage is refilled
+// only when both CTAs' MMAs have released it, so every MMA commit of a stage
+// arrives on that stage's empty barrier in both CTAs.
+//
+// kPair = true (paired-SM MMAs, tcgen05 cta_group::2, M = 256): each CTA loads
+// its own A rows and its own half of B's columns into its own shared memory,
+// signalling the even (leader) CTA's full barrier; the leader's single MMA
+// thread issues M = 256 MMAs that read both CTAs' shared memory and write each
+// CTA's 128 accumulator rows into its own TMEM. Commits multicast to both CTAs;
+// the odd CTA's epilogue releases the accumulator on the leader's barrier.
+template <bool kGram, int kBN, int kStages, int kCluster, bool kFinal, bool kPair = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     ns_gemm_kernel(const __grid_constant__ GemmArgs args, const __grid_constant__ FinalArgs<kFinal ? kMaxFinal : 1> fin) {
-  using S = GemmShape<kGram, kBN, kStages>;
+  using S = GemmShape<kGram, kBN, kStages, kPair>;
   constexpr int BM = S::BM, BK = S::BK;
   constexpr uint32_t A_BYTES = S::A_BYTES, B_BYTES = S::B_BYTES;
-  constexpr uint32_t kIdesc = instr_desc_bf16(BM, kBN, !kGram);
+  constexpr uint32_t kIdesc = instr_desc_bf16(kPair ? 2 * BM : BM, kBN, !kGram);
   constexpr uint16_t kPairMask = 0x3;
+  static_assert(!kPair || kCluster == 2, "paired-SM MMAs need clusters of two");
   static_assert(kBN == 256, "tile width");
   static_assert(kCluster == 1 || kCluster == 2, "cluster size");
   static_assert(!(kGram && kFinal), "only the combine writes to the caller's matrices");
@@ -211,11 +222,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(full_bar(st), 1);
-      mbar_init(empty_bar(st), kCluster);
+      mbar_init(empty_bar(st), kPair ? 1 : kCluster);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpilogueThreads);
+      // Paired: one arrival per epilogue warp of both CTAs, on the leader's barrier.
+      mbar_init(tempty_bar(a), kPair ? 2 * (kEpilogueThreads / 32) : kEpilogueThreads);
     }
     mbar_init(drain_bar, 1);
     for (int w = 0; w < 8; ++w) mbar_init(addend_bar(w), 1);
@@ -232,8 +244,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_u32(tmem_slot), S::TMEM_COLS);  // with warp 1 of the peer CTA
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -265,6 +282,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
+          if constexpr (kPair) {
+            // Both CTAs' loads complete on the leader's full barrier, which expects them all.
+            const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * bytes);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            if (!a_in_b)
+              tma_load_3d_pair(smem_u32(sA + stage * A_BYTES), ma, leader_full, kb * BK, I * BM, td.y);
+            const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
+            if (kGram) {  // this CTA's 128 of the 256 B rows
+              tma_load_3d_pair(b_dst, mb, leader_full, kb * BK, td.w * kBN + rank * 128, td.y);
+            } else {      // this CTA's 128 of the 256 B columns, two boxes of 64
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d_pair(b_dst + c * 8192u, mb, leader_full, td.w * kBN + rank * 128 + c * 64, kb * BK, td.y);
+            }
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(full_bar(stage), bytes);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -290,7 +329,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (!ok) break;
       }
-      if (*abort_flag) {
+      if (*abort_flag && (!kPair || rank == 0)) {
         // Let loads already issued land before the CTA's shared memory is released.
         for (int st = 0; st < kStages; ++st)
           if (armed & (1u << st)) mbar_wait_drain(full_bar(st), (armed_parity >> st) & 1u);
@@ -298,7 +337,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && (!kPair || rank == 0)) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -320,8 +359,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
-          const uint32_t a_addr = a_in_b ? b_addr + static_cast<uint32_t>(I & 1) * A_BYTES
-                                         : smem_u32(sA + stage * A_BYTES);
+          // Paired: each CTA's B half holds its own 128 rows, so an A inside B is the whole half.
+          const uint32_t a_addr =
+              a_in_b ? b_addr + (kPair ? 0u : static_cast<uint32_t>(I & 1) * A_BYTES) : smem_u32(sA + stage * A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             // K-major: the next 16 k-values are 32 bytes further along each 128-byte row.
@@ -329,10 +369,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // MN-major: the next 16 k-values are 16 rows (2048 bytes) further down.
             const uint64_t b_desc = kGram ? smem_desc_sw128(b_addr + k * 32u, 16u, 1024u)
                                           : smem_desc_sw128(b_addr + k * 2048u, 8192u, 1024u);
-            mma_bf16_ss(d_tmem, a_desc, b_desc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (kPair)
+              mma_bf16_ss_pair(d_tmem, a_desc, b_desc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              mma_bf16_ss(d_tmem, a_desc, b_desc, kIdesc, (kb | k) != 0 ? 1u : 0u);
           }
           issued = true;
-          if (kCluster == 2)
+          if constexpr (kPair)
+            mma_commit_pair_multicast(empty_bar(stage), kPairMask);
+          else if (kCluster == 2)
             mma_commit_multicast(empty_bar(stage), kPairMask);
           else
             mma_commit(empty_bar(stage));
@@ -342,14 +387,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(tfull_bar(acc));
+        if constexpr (kPair)
+          mma_commit_pair_multicast(tfull_bar(acc), kPairMask);
+        else
+          mma_commit(tfull_bar(acc));
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       if (*abort_flag && issued) {
-        mma_commit(drain_bar);
+        if constexpr (kPair)
+          mma_commit_pair_multicast(drain_bar, 0x1);
+        else
+          mma_commit(drain_bar);
         mbar_wait_drain(drain_bar, 0);
       }
     }
@@ -533,7 +584,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok) break;
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      if constexpr (kPair) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));  // the leader's barrier
+      } else {
+        mbar_arrive(tempty_bar(acc));
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -551,7 +607,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, S::TMEM_COLS);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, S::TMEM_COLS);
   }
 }
 
