@@ -35,10 +35,11 @@ namespace {
 #ifndef MUON_GEMM_PAIR
 #define MUON_GEMM_PAIR 1
 #endif
-// Paired-SM MMAs (tcgen05 cta_group::2): each CTA holds half of B, so a stage is 32 KB and six fit.
+// Paired-SM MMAs (tcgen05 cta_group::2): each CTA holds half of B, so a stage is 32 KB and five fit
+// beside the 64 KB of epilogue staging.
 constexpr bool kPairMma = MUON_GEMM_PAIR != 0;
-constexpr int kGramBN = 256, kGramStages = kPairMma ? 6 : 4;
-constexpr int kCombBN = 256, kCombStages = kPairMma ? 6 : 4;
+constexpr int kGramBN = 256, kGramStages = kPairMma ? 5 : 3;
+constexpr int kCombBN = 256, kCombStages = kPairMma ? 5 : 3;
 constexpr int kCluster = 2;  // the two CTAs that share one B block
 using GramShape = GemmShape<true, kGramBN, kGramStages, kPairMma>;
 using CombShape = GemmShape<false, kCombBN, kCombStages, kPairMma>;
@@ -509,21 +510,21 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
         // Gram on X_t: both operands are rows of X_t (K-major), output n x n.
         ok &= encode_map(h, &B.gram[t].map_a[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 128);
         B.gram[t].map_b[gi] = B.gram[t].map_a[gi];
-        ok &= encode_map(h, &B.gram[t].map_out[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 32);
-        ok &= encode_map(h, &B.gram[t].map_mirror[gi], pbuf, g.n, g.n, g.count, g.ld_p, 32, 64, false);
+        ok &= encode_map(h, &B.gram[t].map_out[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 128);
+        ok &= encode_map(h, &B.gram[t].map_mirror[gi], pbuf, g.n, g.n, g.count, g.ld_p, 128, 64, false);
         B.gram[t].grp[gi] = GemmGroup{nullptr, nullptr, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
                                       static_cast<int>(g.ld_p), static_cast<int>(ceil_div(g.m, 64))};
         // The same Gram writing A = X X^T into the A buffer (first pass when c != 0).
         B.gram_to_a[t].map_a[gi] = B.gram[t].map_a[gi];
         B.gram_to_a[t].map_b[gi] = B.gram[t].map_b[gi];
         B.gram_to_a[t].grp[gi] = B.gram[t].grp[gi];
-        ok &= encode_map(h, &B.gram_to_a[t].map_out[gi], abuf, g.n, g.n, g.count, g.ld_p, 64, 32);
-        ok &= encode_map(h, &B.gram_to_a[t].map_mirror[gi], abuf, g.n, g.n, g.count, g.ld_p, 32, 64, false);
+        ok &= encode_map(h, &B.gram_to_a[t].map_out[gi], abuf, g.n, g.n, g.count, g.ld_p, 64, 128);
+        ok &= encode_map(h, &B.gram_to_a[t].map_mirror[gi], abuf, g.n, g.n, g.count, g.ld_p, 128, 64, false);
         // Combine: A operand = B (n x n, K-major), B operand = X_t MN-major, out = X_{1-t}, addend X_t.
         ok &= encode_map(h, &B.comb[t].map_a[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 128);
         ok &= encode_map(h, &B.comb[t].map_b[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 64);
-        ok &= encode_map(h, &B.comb[t].map_out[gi], xb[1 - t], g.m, g.n, g.count, g.ld_x, 64, 32);
-        ok &= encode_map(h, &B.comb[t].map_e[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 32);
+        ok &= encode_map(h, &B.comb[t].map_out[gi], xb[1 - t], g.m, g.n, g.count, g.ld_x, 64, 128);
+        ok &= encode_map(h, &B.comb[t].map_e[gi], xb[t], g.m, g.n, g.count, g.ld_x, 64, 128);
         B.comb[t].grp[gi] = GemmGroup{reinterpret_cast<uint16_t*>(xb[t]), nullptr, g.n * g.ld_x, static_cast<int>(g.n),
                                       static_cast<int>(g.m), static_cast<int>(g.ld_x),
                                       static_cast<int>(ceil_div(g.n, 64))};
@@ -531,9 +532,9 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
       // A A pass: operands are rows of A (symmetric), addend A, output B.
       ok &= encode_map(h, &B.gram_aa.map_a[gi], abuf, g.n, g.n, g.count, g.ld_p, 64, 128);
       B.gram_aa.map_b[gi] = B.gram_aa.map_a[gi];
-      ok &= encode_map(h, &B.gram_aa.map_out[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 32);
-      ok &= encode_map(h, &B.gram_aa.map_mirror[gi], pbuf, g.n, g.n, g.count, g.ld_p, 32, 64, false);
-      ok &= encode_map(h, &B.gram_aa.map_e[gi], abuf, g.n, g.n, g.count, g.ld_p, 64, 32);
+      ok &= encode_map(h, &B.gram_aa.map_out[gi], pbuf, g.n, g.n, g.count, g.ld_p, 64, 128);
+      ok &= encode_map(h, &B.gram_aa.map_mirror[gi], pbuf, g.n, g.n, g.count, g.ld_p, 128, 64, false);
+      ok &= encode_map(h, &B.gram_aa.map_e[gi], abuf, g.n, g.n, g.count, g.ld_p, 64, 128);
       B.gram_aa.grp[gi] = GemmGroup{abuf, nullptr, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
                                     static_cast<int>(g.ld_p), static_cast<int>(ceil_div(g.n, 64))};
       if (!ok) {
@@ -832,11 +833,11 @@ bool prepare_final(muon_handle h, Plan& P, const muon_matrix* user, bool update,
     const muon_matrix& u = user[j];
     Plan::UserMap& um = P.user_maps[j];
     if (um.ptr != u.ptr || um.ld != u.ld) {
-      // 32 rows x 64 columns swizzled as the combine's tiles; transposed matrices take the
-      // transposed box, 64 rows x 32 columns, unswizzled.
+      // 128 rows x 64 columns swizzled as the combine's tiles; transposed matrices take the
+      // transposed box, 64 rows x 128 columns, unswizzled.
       const bool ok = mi.transposed
-                          ? encode_map(h, &um.map, u.ptr, mi.cols, mi.rows, 1, u.ld, 32, 64, false)
-                          : encode_map(h, &um.map, u.ptr, mi.cols, mi.rows, 1, u.ld, 64, 32, true);
+                          ? encode_map(h, &um.map, u.ptr, mi.cols, mi.rows, 1, u.ld, 128, 64, false)
+                          : encode_map(h, &um.map, u.ptr, mi.cols, mi.rows, 1, u.ld, 64, 128, true);
       if (!ok) {
         um.ptr = nullptr;
         return false;

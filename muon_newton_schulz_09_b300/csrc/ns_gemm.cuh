@@ -51,9 +51,9 @@ struct GemmGroup {
 struct GemmArgs {
   CUtensorMap map_a[kMaxGroups];  // operand A: K-major, box 64 x 128
   CUtensorMap map_b[kMaxGroups];  // operand B: Gram: same as A; combine: MN-major, box 64 x 64
-  CUtensorMap map_out[kMaxGroups];     // output, box 64 columns x 32 rows, 128-byte swizzle
-  CUtensorMap map_mirror[kMaxGroups];  // Gram output again, box 32 columns x 64 rows, no swizzle
-  CUtensorMap map_e[kMaxGroups];       // addend E, box 64 columns x 32 rows, 128-byte swizzle
+  CUtensorMap map_out[kMaxGroups];     // output, box 64 columns x 128 rows, 128-byte swizzle
+  CUtensorMap map_mirror[kMaxGroups];  // Gram output again, box 128 columns x 64 rows, no swizzle
+  CUtensorMap map_e[kMaxGroups];       // addend E, box 64 columns x 128 rows, 128-byte swizzle
   GemmGroup grp[kMaxGroups];
   const int4* tiles;              // {group, matrix within group, tile row, tile col}
   const int* cta_begin;           // CTA b walks tiles[cta_begin[b] .. cta_begin[b+1])
@@ -68,9 +68,9 @@ struct GemmArgs {
 // The last combine of a call can write its result straight into the caller's
 // bf16 matrices: W <- W - scale * X_k (muon_step) or out <- X_k
 // (muon_orthogonalize). One tensor map per matrix, in the order
-// first[group] + matrix-within-group. trans = 1 when the caller's matrix is
-// X_k^T (rows > cols): its box is then 32 columns x 64 rows, unswizzled, and the
-// tile's values go in transposed.
+// first[group] + matrix-within-group: box 64 columns x 128 rows, 128-byte
+// swizzle; or, with trans = 1 (the caller's matrix is X_k^T, rows > cols),
+// 128 columns x 64 rows, unswizzled, and the tile's values go in transposed.
 constexpr int kMaxFinal = 160;
 
 template <int N>
@@ -160,8 +160,8 @@ struct GemmShape {
   // Paired-SM MMAs: each CTA holds only its half of B's columns.
   static constexpr uint32_t B_BYTES = (kPair ? kBN / 2 : kBN) * BK * 2;
   static constexpr uint32_t TMEM_COLS = 2 * kBN;
-  static constexpr uint32_t STAGING_BYTES = 8 * 4096;  // one 32 x 64 bf16 box per epilogue warp
-  static constexpr uint32_t BAR_BYTES = 8 * (2 * kStages + 5 + 8) + 16;  // + one addend barrier per epilogue warp
+  static constexpr uint32_t STAGING_BYTES = 4 * 16384;  // two 128 x 64 bf16 boxes per column half
+  static constexpr uint32_t BAR_BYTES = 8 * (2 * kStages + 5 + 4) + 16;  // + one barrier per staging box
   // 1024 bytes of slack to align the swizzled tiles to 1024.
   static constexpr uint32_t SMEM_BYTES = 1024 + kStages * (A_BYTES + B_BYTES) + STAGING_BYTES + BAR_BYTES;
 };
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* sB = smem + kStages * A_BYTES;
   uint8_t* staging = sB + kStages * B_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + S::STAGING_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5 + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5 + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
-  auto addend_bar = [&](int w) { return bar0 + 8u * (2 * kStages + 5 + w); };  // epilogue warp w's E box
+  auto addend_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 5 + i); };  // staging box i's TMA load
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(tempty_bar(a), kPair ? 2 * (kEpilogueThreads / 32) : kEpilogueThreads);
     }
     mbar_init(drain_bar, 1);
-    for (int w = 0; w < 8; ++w) mbar_init(addend_bar(w), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(addend_bar(i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -406,21 +406,68 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Eight warps, two per TMEM lane quarter; each drains half of the tile's columns, 64 at a
-    // time, through its own 4 KB staging box in shared memory: the addend E (if any) arrives
-    // there by TMA, the result replaces it in place and leaves by a TMA store.
+    // Eight warps, two per TMEM lane quarter. The four warps of a column half work together on
+    // 128-row x 64-column boxes: each writes its 32 rows into a shared staging box, and one thread
+    // moves the whole 16 KB box with a single TMA operation (addend load, output store, mirrored
+    // store). A half owns two staging boxes; both of a tile's addend loads are in flight before
+    // its accumulator is ready, and a box is rewritten only once the store issued from it has
+    // read it. Named barrier 1 + half keeps the four warps in step.
     constexpr int kHalfCols = kBN / 2;
     constexpr int kBoxes = kHalfCols / 64;
+    static_assert(kBoxes == 2, "one staging box per 64 columns of a half");
     const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter .. +31
     const int half = (warp - 2) >> 2;
+    const bool leader = quarter == 0 && lane == 0;  // issues the half's TMA operations
+    const uint32_t half_bar = 1u + static_cast<uint32_t>(half);
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-    uint8_t* stg = staging + (warp - 2) * 4096;
-    const uint32_t stg_addr = smem_u32(stg);
-    const uint32_t ebar = addend_bar(warp - 2);
-    uint32_t ephase = 0;
-    bool e_pending = false;  // an addend load was issued and not yet waited for
+    uint8_t* const stg_base = staging + half * 32768;
+    const uint32_t bar_base = addend_bar(2 * half);
+    uint32_t box_phase = 0u;    // bit b
+    uint32_t box_pending = 0u;  // bit b: a load into box b was issued and not yet waited for
+    auto stg_box = [&](int b) { return stg_base + b * 16384; };
+    auto box_bar = [&](int b) { return bar_base + 8u * static_cast<uint32_t>(b); };
+    auto sync_half = [&]() { named_barrier_sync(half_bar, 128); };
+    // Loads a 16 KB box into staging box b by TMA, once earlier stores have read it (leader).
+    auto load_box = [&](int b, const CUtensorMap* map, int x, int y, int z, bool wait_all) {
+      if (leader) {
+        if (wait_all)
+          bulk_wait_group_read0();
+        else
+          bulk_wait_group_read<1>();
+        mbar_arrive_expect_tx(box_bar(b), 16384u);
+        tma_load_3d(smem_u32(stg_box(b)), map, box_bar(b), x, y, z);
+      }
+      box_pending |= 1u << b;
+    };
+    auto wait_box = [&](int b) -> bool {
+      if (!mbar_wait_bounded(box_bar(b), (box_phase >> b) & 1u, abort_flag, args.err)) return false;
+      box_phase ^= 1u << b;
+      box_pending &= ~(1u << b);
+      return true;
+    };
+    // Box b has been written by all four warps: the leader stores it through `map` at (x, y, z).
+    auto store_box = [&](int b, const CUtensorMap* map, int x, int y, int z) {
+      fence_proxy_async_smem();
+      sync_half();
+      if (leader) {
+        tma_store_3d(map, smem_u32(stg_box(b)), x, y, z);
+        bulk_commit_group();
+      }
+    };
+    // Box b may be overwritten once the store issued from it has read it: the leader waits, all
+    // four warps meet (`pending`: stores allowed to be still reading, the newest first).
+    auto free_box = [&](bool all) {
+      if (leader) {
+        if (all)
+          bulk_wait_group_read0();
+        else
+          bulk_wait_group_read<1>();
+      }
+      sync_half();
+    };
     int acc = 0;
     uint32_t acc_phase = 0;
+    int ring = 0;  // Gram: staging boxes are used in turn by every store
     for (int t = t_begin; t < t_end; ++t) {
       const int4 td = args.tiles[t];
       const int I = td.z + rank;
@@ -433,30 +480,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool skip = kGram && (block_col < I);
       const bool mirror = kGram && (block_col > I);
       const int col_base = td.w * kBN + half * kHalfCols;
-      const int y0 = I * BM + quarter * 32;
+      const int y_tile = I * BM;
       // X = post * X' with X' the stored operand: the Gram gets post^2 on the product, the
       // combine post on both of its terms.
       const float post = G.post ? __ldg(G.post + td.y) : 1.0f;
       const float s_acc = args.s_acc * (kGram ? post * post : post);
       const float s_e = args.s_e * (kGram ? 1.0f : post);
-      // E box `box` into the staging buffer, once the last store from it has been read.
-      auto load_addend = [&](int box) {
-        if (lane == 0) {
-          bulk_wait_group_read0();
-          mbar_arrive_expect_tx(ebar, 4096u);
-          tma_load_3d(stg_addr, &args.map_e[td.x], ebar, col_base + box * 64, y0, td.y);
-        }
-        e_pending = true;
-      };
-      if (has_e && !skip) load_addend(0);  // lands while this tile's MMAs run
-      if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
+      // Addend boxes (box b of this tile through staging box b): box 0 may reuse its staging box
+      // once all but the latest store have read theirs, box 1 once all have.
+      if (has_e && !skip) {
+        load_box(0, &args.map_e[td.x], col_base, y_tile, td.y, false);
+        load_box(1, &args.map_e[td.x], col_base + 64, y_tile, td.y, true);
+      }
+      // A wait that gives up (and raises the CTA abort flag) does not leave the loop on its own:
+      // every warp of the half goes through the same barriers, and all four leave together after
+      // the end-of-tile barrier below.
+      mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err);
       tc_fence_after();
-      bool ok = true;
       if (!skip) {
 #pragma unroll
         for (int box = 0; box < kBoxes; ++box) {
-          if (has_e && box > 0) load_addend(box);
-          uint32_t packed[32];  // this thread's 64 output values of the box, as bf16 pairs
           float v[64];
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
@@ -467,18 +510,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[cc * 32 + k] = s_acc * __uint_as_float(r[k]);
           }
+          const int x0 = col_base + box * 64;
+          // The staging box for this output: the addend's box, or the next in turn (Gram).
+          const int b = has_e ? box : (ring & 1);
+          // This thread's row of the 128 x 64 box: 16-byte chunk j at position j ^ (row & 7) = j ^ (lane & 7).
+          uint8_t* row_ptr = stg_box(b) + (quarter * 32 + lane) * 128;
           if (has_e) {
-            if (!mbar_wait_bounded(ebar, ephase, abort_flag, args.err)) {
-              ok = false;
-              break;
-            }
-            ephase ^= 1u;
-            e_pending = false;
-            // Row `lane` of the 32 x 64 box: 16-byte chunk j holds columns 8j..8j+7, at position j ^ (lane & 7).
+            wait_box(b);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const uint32_t off = static_cast<uint32_t>(lane) * 128u + static_cast<uint32_t>((j ^ (lane & 7)) * 16);
-              const uint4 w4 = *reinterpret_cast<const uint4*>(stg + off);
+              const uint4 w4 = *reinterpret_cast<const uint4*>(row_ptr + ((j ^ (lane & 7)) * 16));
               const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
               for (int h = 0; h < 4; ++h) {
@@ -486,38 +527,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 v[8 * j + 2 * h + 1] += s_e * bf16_bits_to_float(ww[h] >> 16);
               }
             }
-          } else if (lane == 0) {
-            bulk_wait_group_read0();  // the staging box is free once the previous store has read it
+          } else {
+            free_box(false);  // the store two back from this box has read it
+            ++ring;
           }
-          const int x0 = col_base + box * 64;
           if constexpr (kFinal) {
-            // Straight into the caller's matrix: the box at (x0, y0) of X_k, transposed for trans.
+            // Straight into the caller's matrix: the box at (x0, y_tile) of X_k, transposed for trans.
             const int mi = fin.first[td.x] + td.y;
             const bool tr = fin.trans[mi] != 0;
-            const int ux = tr ? y0 : x0, uy = tr ? x0 : y0;
+            const int ux = tr ? y_tile : x0, uy = tr ? x0 : y_tile;
             if (fin.update) {
-              if (lane == 0) {
-                bulk_wait_group_read0();
-                mbar_arrive_expect_tx(ebar, 4096u);
-                tma_load_3d(stg_addr, &fin.map[mi], ebar, ux, uy, 0);
+              fence_proxy_async_smem();  // the addend reads above come before the load's writes
+              sync_half();
+              if (leader) {
+                mbar_arrive_expect_tx(box_bar(b), 16384u);
+                tma_load_3d(smem_u32(stg_box(b)), &fin.map[mi], box_bar(b), ux, uy, 0);
               }
-              e_pending = true;
-              if (!mbar_wait_bounded(ebar, ephase, abort_flag, args.err)) {
-                ok = false;
-                break;
-              }
-              ephase ^= 1u;
-              e_pending = false;
-            } else if (lane == 0) {
-              bulk_wait_group_read0();
+              box_pending |= 1u << b;
+              wait_box(b);
             }
-            __syncwarp();
             const float us = fin.scale[mi];
             if (!tr) {
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const uint32_t off = static_cast<uint32_t>(lane) * 128u + static_cast<uint32_t>((j ^ (lane & 7)) * 16);
-                uint4* p = reinterpret_cast<uint4*>(stg + off);
+                uint4* p = reinterpret_cast<uint4*>(row_ptr + ((j ^ (lane & 7)) * 16));
                 uint32_t ww[4] = {0u, 0u, 0u, 0u};
                 if (fin.update) {
                   const uint4 w4 = *p;
@@ -534,55 +567,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 *p = make_uint4(o[0], o[1], o[2], o[3]);
               }
             } else {
-              uint16_t* p = reinterpret_cast<uint16_t*>(stg);  // 64 rows x 32 columns
+              // 64 rows (the box's columns) x 128 columns (the tile's rows), unswizzled.
+              uint16_t* p = reinterpret_cast<uint16_t*>(stg_box(b));
 #pragma unroll
               for (int c = 0; c < 64; ++c) {
-                const int idx = c * 32 + lane;
+                const int idx = c * 128 + quarter * 32 + lane;
                 p[idx] = fin.update ? to_bf16_bits(bf16_bits_to_float(p[idx]) - us * v[c]) : to_bf16_bits(v[c]);
               }
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_3d(&fin.map[mi], stg_addr, ux, uy, 0);
-              bulk_commit_group();
-            }
+            store_box(b, &fin.map[mi], ux, uy, 0);
           } else {
-          __syncwarp();
+            uint32_t packed[32];  // this thread's 64 output values of the box, as bf16 pairs
 #pragma unroll
-          for (int k = 0; k < 32; ++k) packed[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+            for (int k = 0; k < 32; ++k) packed[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t off = static_cast<uint32_t>(lane) * 128u + static_cast<uint32_t>((j ^ (lane & 7)) * 16);
-            *reinterpret_cast<uint4*>(stg + off) =
-                make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&args.map_out[td.x], stg_addr, x0, y0, td.y);
-            bulk_commit_group();
-          }
-          if (mirror) {
-            // The transposed box: 64 rows (this box's columns) x 32 columns (the warp's rows), unswizzled.
-            if (lane == 0) bulk_wait_group_read0();
-            __syncwarp();
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(row_ptr + ((j ^ (lane & 7)) * 16)) =
+                  make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+            store_box(b, &args.map_out[td.x], x0, y_tile, td.y);
+            if (mirror) {
+              // The transposed box: 64 rows (this box's columns) x 128 columns (the tile's rows),
+              // unswizzled. Without an addend it goes through the next staging box in turn; with
+              // one (the A A pass), the other box may still hold the next addend, so it reuses
+              // this box once the store just issued from it has read it.
+              int bm = b;
+              if (has_e) {
+                free_box(true);
+              } else {
+                bm = ring & 1;
+                ++ring;
+                free_box(false);
+              }
+              uint16_t* p = reinterpret_cast<uint16_t*>(stg_box(bm));
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              reinterpret_cast<uint16_t*>(stg + (2 * k) * 64)[lane] = static_cast<uint16_t>(packed[k] & 0xFFFFu);
-              reinterpret_cast<uint16_t*>(stg + (2 * k + 1) * 64)[lane] = static_cast<uint16_t>(packed[k] >> 16);
+              for (int k = 0; k < 32; ++k) {
+                p[(2 * k) * 128 + quarter * 32 + lane] = static_cast<uint16_t>(packed[k] & 0xFFFFu);
+                p[(2 * k + 1) * 128 + quarter * 32 + lane] = static_cast<uint16_t>(packed[k] >> 16);
+              }
+              store_box(bm, &args.map_mirror[td.x], y_tile, x0, td.y);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_3d(&args.map_mirror[td.x], stg_addr, y0, x0, td.y);
-              bulk_commit_group();
-            }
-          }
           }
         }
       }
-      if (!ok) break;
+      sync_half();  // the abort flag, if raised in this tile, is seen by all four warps alike
+      if (*abort_flag) break;
       tc_fence_before();
       if constexpr (kPair) {
         __syncwarp();
@@ -595,9 +623,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         acc_phase ^= 1u;
       }
     }
-    if (lane == 0) {
-      if (e_pending) mbar_wait_drain(ebar, ephase);  // abort path: let the addend load land
-      bulk_wait_group0();  // every store of this warp has reached global memory
+    if (leader) {
+      for (int b = 0; b < 2; ++b)  // abort path: let loads land
+        if ((box_pending >> b) & 1u) mbar_wait_drain(box_bar(b), (box_phase >> b) & 1u);
+      bulk_wait_group0();  // every store of this half has reached global memory
     }
   }
 
