@@ -25,7 +25,11 @@ stated configuration:
 3. orient:    X = X0^T when rows > cols (square matrices are not transposed)
 4. iterate k times:  A = X X^T;  B = b*A + c*A*A;  X <- a*X + B X
 5. restore:   O = X^T if transposed in step 3
-6. update:    W <- W - lr * max(1, rows/cols)^0.5 * O
+6. update:    W <- W * (1 - lr * wd) - lr * max(1, rows/cols)^0.5 * O
+
+The weight decay wd (0 unless given) follows the energy-efficiency article on
+Modded-NanoGPT (hyperparameter paragraph), which reports wd = 1.0 without its
+form; the decoupled form above is the plainest reading.
 
 Everything is float64. Matrix products use numpy's matmul, a library
 primitive. There is no blocking, fusion or reordering beyond the steps as
@@ -93,19 +97,20 @@ def lr_scale(rows: int, cols: int) -> float:
     return max(1.0, rows / cols) ** 0.5
 
 
-def muon_update(w, o, lr: float, scale_lr_by_shape: bool = True):
-    """Step 6. W - lr * s * O in float64, where s is lr_scale or 1."""
+def muon_update(w, o, lr: float, scale_lr_by_shape: bool = True, weight_decay: float = 0.0):
+    """Step 6. W (1 - lr*wd) - lr * s * O in float64, where s is lr_scale or 1."""
     w = np.asarray(w, dtype=np.float64)
     s = lr_scale(*w.shape) if scale_lr_by_shape else 1.0
-    return w - (lr * s) * np.asarray(o, dtype=np.float64)
+    return w * (1.0 - lr * weight_decay) - (lr * s) * np.asarray(o, dtype=np.float64)
 
 
 def muon_step(w, g, buf, lr: float, beta: float, nesterov: bool, steps: int = 5,
-              coeffs=DEFAULT_COEFFS, eps: float = DEFAULT_EPS, scale_lr_by_shape: bool = True):
+              coeffs=DEFAULT_COEFFS, eps: float = DEFAULT_EPS, scale_lr_by_shape: bool = True,
+              weight_decay: float = 0.0):
     """One full Muon step for one matrix. Returns (W_new, buf_new, O), all float64."""
     buf_new, u = momentum(g, buf, beta, nesterov)
     o = orthogonalize(u, steps, coeffs, eps)
-    return muon_update(w, o, lr, scale_lr_by_shape), buf_new, o
+    return muon_update(w, o, lr, scale_lr_by_shape, weight_decay), buf_new, o
 
 
 def rel_frobenius(x, ref) -> float:

@@ -241,6 +241,36 @@ def test_lr_scale_via_step():
     np.testing.assert_allclose(w_new, -0.5 * math.sqrt(3.0) * g / 3.0, atol=1e-15)
 
 
+def test_weight_decay_closed_form():
+    """W' = W (1 - lr wd) - lr s O, element by element: a 1x2 row (no transpose, s = 1) whose
+    orthogonalised update is g/|g| exactly (a single row is its own polar factor at any step count)."""
+    w = np.array([[2.0, -4.0]])
+    g = np.array([[3.0, 4.0]])
+    lr, wd = 0.1, 1.0
+    w_new, _, o = mo.muon_step(w, g, np.zeros((1, 2)), lr, 0.0, False, 3, CUBIC, 0.0, True, wd)
+    np.testing.assert_allclose(o, g / 5.0, atol=1e-15)
+    np.testing.assert_allclose(w_new, [[2.0 * 0.9 - 0.1 * 0.6, -4.0 * 0.9 - 0.1 * 0.8]], atol=1e-15)
+    # wd = 0 leaves the plain update
+    w0, _, _ = mo.muon_step(w, g, np.zeros((1, 2)), lr, 0.0, False, 3, CUBIC, 0.0, True, 0.0)
+    np.testing.assert_allclose(w0, w - lr * g / 5.0, atol=1e-15)
+
+
+def test_pins_catch_planted_weight_decay_mistakes(monkeypatch):
+    def coupled(w, o, lr, scale_lr_by_shape=True, weight_decay=0.0):  # decay without the lr factor
+        s = mo.lr_scale(*np.shape(w)) if scale_lr_by_shape else 1.0
+        return np.asarray(w, np.float64) * (1.0 - weight_decay) - lr * s * np.asarray(o, np.float64)
+
+    def on_update(w, o, lr, scale_lr_by_shape=True, weight_decay=0.0):  # decay applied to O, not W
+        s = mo.lr_scale(*np.shape(w)) if scale_lr_by_shape else 1.0
+        return np.asarray(w, np.float64) - lr * s * (1.0 + weight_decay) * np.asarray(o, np.float64)
+
+    for fn in (coupled, on_update):
+        with monkeypatch.context() as m:
+            m.setattr(mo, "muon_update", fn)
+            with pytest.raises(AssertionError):
+                test_weight_decay_closed_form()
+
+
 @pytest.mark.parametrize("case", golden()["muon_step"], ids=lambda c: c["name"])
 def test_golden_muon_step(case):
     w = np.array(case["W"], np.float64)
@@ -347,9 +377,9 @@ def test_pins_catch_planted_step_mistakes(monkeypatch):
         nb = beta * buf + g
         return nb, (beta * nb if nesterov else nb)
 
-    def upd_plus(w, o, lr, scale_lr_by_shape=True):
+    def upd_plus(w, o, lr, scale_lr_by_shape=True, weight_decay=0.0):
         s = mo.lr_scale(*np.shape(w)) if scale_lr_by_shape else 1.0
-        return np.asarray(w, np.float64) + lr * s * np.asarray(o, np.float64)
+        return np.asarray(w, np.float64) * (1.0 - lr * weight_decay) + lr * s * np.asarray(o, np.float64)
 
     def scale_inverted(rows, cols):
         return max(1.0, cols / rows) ** 0.5
