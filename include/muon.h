@@ -19,7 +19,7 @@
  *   3. orient     X = X0^T when rows > cols (n = min(rows,cols) <= m = max)
  *   4. iterate    A = X X^T;  B = b*A + c*A*A;  X <- a*X + B X      (k times)
  *   5. restore    O = X^T if step 3 transposed, else X
- *   6. update     W <- W - lr * s * O,  s = max(1, rows/cols)^0.5 (or 1)
+ *   6. update     W <- W * (1 - lr * wd) - lr * s * O,  s = max(1, rows/cols)^0.5 (or 1)
  *
  * muon_step runs 1-6, muon_orthogonalize runs 2-5.
  *
@@ -85,17 +85,21 @@ typedef struct {
  * steps: iterations k (>= 0). a, b, c: the odd polynomial a*x + b*x^3 + c*x^5
  * applied to the singular values. eps: added to ||u||_F, outside the square
  * root. scale_lr_by_shape: nonzero applies s = max(1, rows/cols)^0.5 in step 6,
- * zero applies s = 1. */
+ * zero applies s = 1. weight_decay (>= 0): decoupled decay, step 6 becomes
+ * W <- W * (1 - lr * weight_decay) - lr * s * O. The energy-efficiency article
+ * on Modded-NanoGPT (hyperparameter paragraph) reports wd = 1.0; the form is
+ * this library's reading. */
 typedef struct {
   int32_t steps;
   float a, b, c;
   float eps;
   int32_t scale_lr_by_shape;
+  float weight_decay;
 } muon_config;
 
 /* Fills *cfg with the defaults: steps 5, (a,b,c) = (1.5, -0.5, 0), eps 1e-7,
- * scale_lr_by_shape 1. The cubic coefficients are the iteration's textbook
- * form; the pages give none. */
+ * scale_lr_by_shape 1, weight_decay 0. The cubic coefficients are the
+ * iteration's textbook form; the pages give none. */
 void muon_default_config(muon_config* cfg);
 
 /* Creates a handle on CUDA device `device`. cfg may be NULL (defaults).
@@ -119,7 +123,7 @@ muon_status muon_orthogonalize(muon_handle h, const muon_matrix* in, const muon_
 /* Steps 1-6 on `count` matrices with the handle's Newton-Schulz settings:
  *   momentum[j] <- beta*momentum[j] + grads[j]
  *   u = grads[j] + beta*momentum[j]   (nesterov != 0)   or   u = momentum[j]
- *   params[j]  <- params[j] - lr * s_j * NS_k(u)
+ *   params[j]  <- params[j] * (1 - lr * weight_decay) - lr * s_j * NS_k(u)
  * params: F32 or BF16 (all alike). grads: F32 or BF16 (all alike).
  * momentum: F32. All three of matrix j have the same rows and cols and must
  * not overlap one another. count == 0 is a no-op. */

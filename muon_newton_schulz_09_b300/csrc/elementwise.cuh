@@ -379,23 +379,25 @@ struct MapMat {
 struct MapArgs {
   MapMat m[kEwMax];
   int count;
+  float keep;  // kUpdate: 1 - lr * weight_decay, applied to the old destination
 };
 
 template <int kMode, bool kDstF32>
-__device__ __forceinline__ void map_apply1(const MapMat& M, float f, float s, int64_t di) {
+__device__ __forceinline__ void map_apply1(const MapMat& M, float f, float s, int64_t di, float keep) {
   if (kMode == kUpdate)
-    store1<kDstF32>(M.dst, di, load1<kDstF32>(M.dst, di) - f * s);
+    store1<kDstF32>(M.dst, di, keep * load1<kDstF32>(M.dst, di) - f * s);
   else
     store1<kDstF32>(M.dst, di, (kMode == kScale) ? s * f : s);
 }
 
 // d = f(s) for eight elements: the old destination values dold are used by kUpdate only.
 template <int kMode>
-__device__ __forceinline__ void map_combine8(float f, const float (&sv)[8], const float (&dold)[8], float (&d)[8]) {
+__device__ __forceinline__ void map_combine8(float f, const float (&sv)[8], const float (&dold)[8], float (&d)[8],
+                                             float keep) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     if (kMode == kUpdate)
-      d[k] = dold[k] - f * sv[k];
+      d[k] = keep * dold[k] - f * sv[k];
     else if (kMode == kScale)
       d[k] = sv[k] * f;
     else
@@ -438,14 +440,14 @@ __global__ void __launch_bounds__(kEwThreads, 3) map_kernel(const __grid_constan
           float sv[8], dold[8], d[8];
           unpack8<kSrcF32>(sr[v], sv);
           if (kMode == kUpdate) unpack8<kDstF32>(dr[v], dold);
-          map_combine8<kMode>(f, sv, dold, d);
+          map_combine8<kMode>(f, sv, dold, d, a.keep);
           store8<kDstF32>(M.dst, e, d);
         }
       }
     } else {
       for (int64_t e = e0 + threadIdx.x; e < e1; e += kEwThreads) {
         const int64_t row = e / cols, col = e - row * cols;
-        map_apply1<kMode, kDstF32>(M, f, load1<kSrcF32>(M.src, row * M.ld_src + col), row * M.ld_dst + col);
+        map_apply1<kMode, kDstF32>(M, f, load1<kSrcF32>(M.src, row * M.ld_src + col), row * M.ld_dst + col, a.keep);
       }
     }
     return;
@@ -506,12 +508,12 @@ __global__ void __launch_bounds__(kEwThreads, 3) map_kernel(const __grid_constan
     if (M.vec_ok && dc + 7 < M.sr) {
       float dold[8], d[8];
       if (kMode == kUpdate) unpack8<kDstF32>(draw[p], dold);
-      map_combine8<kMode>(f, sv, dold, d);
+      map_combine8<kMode>(f, sv, dold, d, a.keep);
       store8<kDstF32>(M.dst, di, d);
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (dc + k < M.sr) map_apply1<kMode, kDstF32>(M, f, sv[k], di + k);
+        if (dc + k < M.sr) map_apply1<kMode, kDstF32>(M, f, sv[k], di + k, a.keep);
     }
   }
 }

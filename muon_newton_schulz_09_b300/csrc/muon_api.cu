@@ -710,6 +710,7 @@ muon_status launch_map(muon_handle h, const Plan& P, const muon_matrix* user, in
     }
   MapArgs a;
   memset(&a, 0, sizeof(a));
+  a.keep = (kMode == kUpdate) ? 1.0f - lr * h->cfg.weight_decay : 1.0f;
   int blocks = 0;
   bool src_f32 = false, dst_f32 = false;
   auto flush = [&]() -> muon_status {
@@ -826,6 +827,7 @@ bool prepare_final(muon_handle h, Plan& P, const muon_matrix* user, bool update,
     }
     if (running > kMaxFinal) return false;
     F.update = update ? 1 : 0;
+    F.keep = update ? 1.0f - lr * h->cfg.weight_decay : 1.0f;
   }
   for (size_t j = 0; j < P.mats.size(); ++j) {
     const MatInfo& mi = P.mats[j];
@@ -947,6 +949,7 @@ void muon_default_config(muon_config* cfg) {
   cfg->c = 0.0f;
   cfg->eps = 1e-7f;
   cfg->scale_lr_by_shape = 1;
+  cfg->weight_decay = 0.0f;
 }
 
 const char* muon_status_string(muon_status s) {
@@ -1092,7 +1095,8 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
   if (!out) return MUON_ERR_INVALID;
   *out = nullptr;
   if (cfg && (cfg->steps < 0 || cfg->steps > kMaxSteps || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->a) ||
-              !std::isfinite(cfg->b) || !std::isfinite(cfg->c)))
+              !std::isfinite(cfg->b) || !std::isfinite(cfg->c) || !(cfg->weight_decay >= 0.0f) ||
+              !std::isfinite(cfg->weight_decay)))
     return MUON_ERR_INVALID;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) {

@@ -123,6 +123,7 @@ extern "C" muon_status muon_normalize_noalloc(const muon_matrix* in, const muon_
   memset(&na, 0, sizeof(na));
   memset(&ma, 0, sizeof(ma));
   na.eps = eps;
+  ma.keep = 1.0f;
   int nblocks = 0, mblocks = 0;
   int64_t part_off = 0;
   for (int j = 0; j < count; ++j) {

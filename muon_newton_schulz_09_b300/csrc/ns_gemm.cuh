@@ -79,7 +79,8 @@ struct FinalArgs {
   float scale[N];
   uint8_t trans[N];
   int first[kMaxGroups];
-  int update;  // 1: W <- W - scale * X_k; 0: out <- X_k
+  int update;  // 1: W <- keep * W - scale * X_k; 0: out <- X_k
+  float keep;  // 1 - lr * weight_decay
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -560,8 +561,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                   const float lo = v[8 * j + 2 * h], hi = v[8 * j + 2 * h + 1];
-                  o[h] = fin.update ? pack_bf16x2(bf16_bits_to_float(ww[h] & 0xFFFFu) - us * lo,
-                                                  bf16_bits_to_float(ww[h] >> 16) - us * hi)
+                  o[h] = fin.update ? pack_bf16x2(fin.keep * bf16_bits_to_float(ww[h] & 0xFFFFu) - us * lo,
+                                                  fin.keep * bf16_bits_to_float(ww[h] >> 16) - us * hi)
                                     : pack_bf16x2(lo, hi);
                 }
                 *p = make_uint4(o[0], o[1], o[2], o[3]);
@@ -572,7 +573,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
               for (int c = 0; c < 64; ++c) {
                 const int idx = c * 128 + quarter * 32 + lane;
-                p[idx] = fin.update ? to_bf16_bits(bf16_bits_to_float(p[idx]) - us * v[c]) : to_bf16_bits(v[c]);
+                p[idx] = fin.update ? to_bf16_bits(fin.keep * bf16_bits_to_float(p[idx]) - us * v[c])
+                                    : to_bf16_bits(v[c]);
               }
             }
             store_box(b, &fin.map[mi], ux, uy, 0);

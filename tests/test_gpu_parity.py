@@ -226,6 +226,27 @@ def test_step_zero_iterations_is_normalised_momentum():
         assert rel_f(-host(P[j]) / oracle.lr_scale(r, c), want) < 4e-3
 
 
+@pytest.mark.parametrize("param_dtype", ["bf16", "f32"], ids=["fused", "kernel"])
+def test_step_weight_decay(param_dtype):
+    """Decoupled weight decay wd = 1.0: W' = W (1 - lr wd) - lr s O. bf16 params take the update fused
+    into the last combine, fp32 params the separate update kernel."""
+    from muon_newton_schulz_09_b300 import Muon
+    shapes = [(256, 640), (640, 256), (130, 70)]
+    w, g, m, p = step_case(shapes, "bf16", param_dtype, seed=26)
+    lr, wd = 0.02, 1.0
+    P = [dev(x, param_dtype) for x in p]
+    with Muon(0, weight_decay=wd) as mw:
+        mw.step(P, [dev(x, "bf16") for x in g], [dev(x, "f32") for x in m], lr=lr, beta=0.95, nesterov=True)
+        torch.cuda.synchronize()
+        assert mw.get_error() == 0
+    for j, (r, c) in enumerate(shapes):
+        w_new, _, o = oracle.muon_step(p[j], g[j], m[j], lr, 0.95, True, 5, CUBIC, weight_decay=wd)
+        upd = lr * oracle.lr_scale(r, c) * np.abs(o).max()
+        err = np.abs(host(P[j]) - w_new)
+        ulp = bf16_ulp(w_new) if param_dtype == "bf16" else np.abs(w_new) * 2.0 ** -22
+        assert np.all(err <= ulp + 0.05 * upd), (r, c, float(err.max()))
+
+
 def test_step_f32_grads_config1(muon):
     """One fp32 128x256 gradient N(0,1), zero momentum, beta 0.95, 5 cubic iterations."""
     w = wl.SINGLE_128x256
