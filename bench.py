@@ -37,7 +37,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch of each kernel from one ncu capture, keyed
 # by the hash of the kernel sources they were taken with. A stale hash gives null.
 NCU_TRAFFIC = {
-    "3159a03b4c84e9a1": {"combine_ax_bx": 388.9e6, "gram_xxt": 211.7e6},  # ncu --set full, GPT-2 124M set
+    "fc24e113884ea847": {"combine_ax_bx": 390.4e6, "gram_xxt": 210.3e6,  # ncu --set full, GPT-2 124M set
+                         "gram_aa": 126.5e6},  # the same set with the quintic
 }
 
 KERNEL_SOURCES = ["muon_newton_schulz_09_b300/csrc/ns_gemm.cuh", "muon_newton_schulz_09_b300/csrc/elementwise.cuh",

@@ -64,6 +64,16 @@ def test_gpt2_350m_full_step(muon):
     print("gpt2_350m rel-F per sampled matrix:", errs)
 
 
+def test_gpt2_124m_quintic_step():
+    """The c != 0 path (an A A Gram pass with b A in its epilogue) in the benchmark's launch configuration."""
+    from muon_newton_schulz_09_b300 import Muon
+    w = wl.GPT2_124M_QUINTIC
+    a, b, c = w.coeffs
+    with Muon(0, steps=w.steps, a=a, b=b, c=c) as mq:
+        errs = _step_check(mq, w, sample=[0, 4, 5, 71])
+    print("gpt2_124m quintic rel-F per sampled matrix:", errs)
+
+
 def test_square_64x1024(muon):
     w = wl.SQUARE_64x1024
     dw = bench.DeviceWorkload(w, 0)
