@@ -33,6 +33,9 @@ import workloads as wl  # noqa: E402
 METRIC = "Muon steps/sec at GPT-2 124M hidden-matrix shapes; % BF16 TC peak, HBM GB/s"
 UNIT = "steps/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# Dense bf16 tensor rate per SM and clock: 2.25 PFLOP/s nominal = 148 SMs x 8192 flops x 1.86 GHz.
+DENSE_FLOPS_PER_SM_CYCLE = 8192
+SMS = 148
 
 # DRAM bytes (read + write) per launch of each kernel from one ncu capture, keyed
 # by the hash of the kernel sources they were taken with. A stale hash gives null.
@@ -439,6 +442,9 @@ def run_ours(args) -> dict:
     barrier()
     muon.profile(False)
     prof = muon.profile_read()
+    # The SM clock the GEMM kernels themselves saw: clock64 cycles over %globaltimer ns, summed over
+    # their CTAs. nvidia-smi samples every 200 ms and misses the power-cap dips inside a step.
+    device_mhz = muon.profile_clock()
     prof_s = p0.elapsed_time(p1) / 1e3
     if muon.get_error() != 0:
         raise RuntimeError("device error flag raised during the profiled region")
@@ -457,7 +463,9 @@ def run_ours(args) -> dict:
     peaks, peak_src = load_peaks()
     # The sustained tensor peak applies when the region ran long or under the power cap.
     clk = clk.summary()
-    sustained = prof_s >= 1.0 or "sw_power_cap" in clk.get("reasons", [])
+    clk["sm_mhz_device"] = round(device_mhz, 1)
+    sustained = (prof_s >= 1.0 or "sw_power_cap" in clk.get("reasons", [])
+                 or (0 < device_mhz < 0.9 * clk.get("sm_max_mhz", peaks.get("sm_max_mhz", 2032.0))))
     tc_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
     work = kernel_work(w)
     kernels = {}
@@ -472,6 +480,8 @@ def run_ours(args) -> dict:
             kernels[name] = {"launches": n, "avg_us": avg_ms * 1e3, "share": 0.0, "bound": "tensor",
                              "achieved": ach, "unit": "TFLOP/s", "frac": ach / tc_peak,
                              "frac_burst": ach / peaks["bf16_tflops"]}
+            if device_mhz > 0:  # of the dense rate at the clock the kernels ran at
+                kernels[name]["frac_per_cycle"] = ach / (DENSE_FLOPS_PER_SM_CYCLE * SMS * device_mhz * 1e6 / 1e12)
         else:
             ach = amount / (avg_ms * 1e-3) / 1e9
             kernels[name] = {"launches": n, "avg_us": avg_ms * 1e3, "share": 0.0, "bound": "hbm",

@@ -180,6 +180,12 @@ muon_status muon_selftest_wait(muon_handle h, int64_t limit_ns, void* stream);
 muon_status muon_profile_enable(muon_handle h, int enable);
 muon_status muon_profile_read(muon_handle h, double* ms, int64_t* launches);
 const char* muon_kernel_name(int kind);
+/* The SM clock the tensor-core GEMM kernels ran at while profiling was on:
+ * their CTAs' summed clock64() cycles over their summed %globaltimer
+ * nanoseconds, in MHz (0 if none ran). muon_profile_enable(h, 1) resets the
+ * sums when it turns profiling on. Synchronous: call it after
+ * muon_profile_read, which waits for the profiled kernels. */
+muon_status muon_profile_clock(muon_handle h, double* sm_mhz);
 
 /* ---------------------------------------------------------------- allocation-free normalisation
  * The pages have no counterpart to this entry point. It exists for callers

@@ -74,6 +74,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                       P(c.c_int64), P(c.c_double)]),
         "muon_profile_enable": (c.c_int, [c.c_void_p, c.c_int]),
         "muon_profile_read": (c.c_int, [c.c_void_p, P(c.c_double), P(c.c_int64)]),
+        "muon_profile_clock": (c.c_int, [c.c_void_p, P(c.c_double)]),
         "muon_kernel_name": (c.c_char_p, [c.c_int]),
         "muon_selftest_wait": (c.c_int, [c.c_void_p, c.c_int64, c.c_void_p]),
         "muon_normalize_noalloc": (c.c_int, [P(MuonMatrix), P(MuonMatrix), c.c_int, c.c_float, c.c_void_p,
@@ -269,6 +270,12 @@ class Muon:
         n = (ctypes.c_int64 * KERNEL_KINDS)()
         self._check(self.lib.muon_profile_read(self.handle, ms, n), "muon_profile_read")
         return {kernel_name(k): (ms[k], n[k]) for k in range(KERNEL_KINDS)}
+
+    def profile_clock(self) -> float:
+        """MHz of the SM clock under the GEMM kernels profiled since profiling was turned on."""
+        v = ctypes.c_double()
+        self._check(self.lib.muon_profile_clock(self.handle, ctypes.byref(v)), "muon_profile_clock")
+        return v.value
 
     def close(self):
         if getattr(self, "handle", None):

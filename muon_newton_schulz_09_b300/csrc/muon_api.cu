@@ -190,7 +190,8 @@ struct muon_ctx {
   int num_sms = 0;
   int max_lists = 0;  // GEMM tile lists run at once: co-resident clusters (or CTAs)
   muon_config cfg{};
-  int* err_dev = nullptr;
+  int* err_dev = nullptr;            // 256 bytes: the error flag at 0, the profiling clock sums at 64
+  unsigned long long* clk_dev = nullptr;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   std::map<std::vector<std::pair<int64_t, int64_t>>, std::unique_ptr<Plan>> plans;
   uint64_t use_clock = 0;
@@ -793,7 +794,14 @@ muon_status launch_gemm(muon_handle h, const GemmArgs& a, const FinalArgs<kFinal
   ProfScope ps(h, kind, s);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = gemm_config<kGram, kBN, kStages>(a.grid, s, attr);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kCluster, kFinal, kPairMma>, a, f);
+  cudaError_t e;
+  if (h->profiling) {
+    GemmArgs ap = a;
+    ap.clk = h->clk_dev;
+    e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kCluster, kFinal, kPairMma>, ap, f);
+  } else {
+    e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kCluster, kFinal, kPairMma>, a, f);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(h, e, "tcgen05 GEMM launch");
@@ -1127,6 +1135,7 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
     cudaFree(h->err_dev);
     return MUON_ERR_CUDA;
   }
+  h->clk_dev = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(h->err_dev) + 64);
   auto kgram = ns_gemm_kernel<true, kGramBN, kGramStages, kCluster, false, kPairMma>;
   auto kcomb = ns_gemm_kernel<false, kCombBN, kCombStages, kCluster, false, kPairMma>;
   auto kfinal = ns_gemm_kernel<false, kCombBN, kCombStages, kCluster, true, kPairMma>;
@@ -1251,7 +1260,26 @@ muon_status muon_selftest_wait(muon_handle h, int64_t limit_ns, void* stream) {
 
 muon_status muon_profile_enable(muon_handle h, int enable) {
   if (!h) return MUON_ERR_INVALID;
+  if (enable && !h->profiling) {
+    DeviceGuard guard(h->device);
+    if (cudaMemset(h->clk_dev, 0, 2 * sizeof(unsigned long long)) != cudaSuccess) {
+      cudaGetLastError();
+      return MUON_ERR_CUDA;
+    }
+  }
   h->profiling = enable != 0;
+  return MUON_OK;
+}
+
+muon_status muon_profile_clock(muon_handle h, double* sm_mhz) {
+  if (!h || !sm_mhz) return MUON_ERR_INVALID;
+  DeviceGuard guard(h->device);
+  unsigned long long v[2] = {0, 0};
+  if (cudaMemcpy(v, h->clk_dev, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MUON_ERR_CUDA;
+  }
+  *sm_mhz = v[1] ? 1e3 * static_cast<double>(v[0]) / static_cast<double>(v[1]) : 0.0;
   return MUON_OK;
 }
 

@@ -63,6 +63,7 @@ struct GemmArgs {
   float s_acc;
   float s_e;
   int* err;
+  unsigned long long* clk;  // non-null while profiling: += {SM cycles, ns} of every CTA of the launch
 };
 
 // The last combine of a call can write its result straight into the caller's
@@ -195,6 +196,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   static_assert(!(kGram && kFinal), "only the combine writes to the caller's matrices");
   static_assert(S::TMEM_COLS == 512, "TMEM allocation must be a power of two");
 
+  const long long clk_start = clock64();
+  const uint64_t ns_start = global_timer_ns();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -498,7 +501,95 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // the end-of-tile barrier below.
       mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err);
       tc_fence_after();
-      if (!skip) {
+      bool released = false;  // the accumulator has been handed back to the MMA warp
+      if constexpr (kFinal) {
+        // The last combine writes straight into the caller's matrices. Both boxes of X_k are first
+        // taken into registers as bf16 (the value the workspace would have held), the accumulator
+        // is released at once, and only then are the caller's two boxes loaded in place of the
+        // addends, both in flight together: W' = keep * W - scale * X_k, or out = X_k.
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int box = 0; box < kBoxes; ++box) {
+          float v[64];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t r[32];
+            tmem_load_32cols(
+                tmem_base + lane_field + static_cast<uint32_t>(acc * kBN + half * kHalfCols + box * 64 + cc * 32), r);
+            tmem_load_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[cc * 32 + k] = s_acc * __uint_as_float(r[k]);
+          }
+          const uint8_t* row_ptr = stg_box(box) + (quarter * 32 + lane) * 128;
+          wait_box(box);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 w4 = *reinterpret_cast<const uint4*>(row_ptr + ((j ^ (lane & 7)) * 16));
+            const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+              pk[box][4 * j + h] = pack_bf16x2(v[8 * j + 2 * h] + s_e * bf16_bits_to_float(ww[h] & 0xFFFFu),
+                                               v[8 * j + 2 * h + 1] + s_e * bf16_bits_to_float(ww[h] >> 16));
+          }
+        }
+        tc_fence_before();
+        if constexpr (kPair) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));  // the leader's barrier
+        } else {
+          mbar_arrive(tempty_bar(acc));
+        }
+        released = true;
+        const int mi = fin.first[td.x] + td.y;
+        const bool tr = fin.trans[mi] != 0;
+        const float us = fin.scale[mi];
+        if (fin.update) {
+          fence_proxy_async_smem();  // the addend reads above come before the loads' writes
+          sync_half();
+#pragma unroll
+          for (int box = 0; box < kBoxes; ++box) {
+            const int x0 = col_base + box * 64;
+            if (leader) {
+              mbar_arrive_expect_tx(box_bar(box), 16384u);
+              tma_load_3d(smem_u32(stg_box(box)), &fin.map[mi], box_bar(box), tr ? y_tile : x0, tr ? x0 : y_tile, 0);
+            }
+            box_pending |= 1u << box;
+          }
+        }
+#pragma unroll
+        for (int box = 0; box < kBoxes; ++box) {
+          const int x0 = col_base + box * 64;
+          if (fin.update) wait_box(box);
+          if (!tr) {
+            // The box at (x0, y_tile), swizzled like the addend: this thread's row, chunk j at j ^ (lane & 7).
+            uint8_t* row_ptr = stg_box(box) + (quarter * 32 + lane) * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint4* q = reinterpret_cast<uint4*>(row_ptr + ((j ^ (lane & 7)) * 16));
+              uint32_t o[4] = {pk[box][4 * j], pk[box][4 * j + 1], pk[box][4 * j + 2], pk[box][4 * j + 3]};
+              if (fin.update) {
+                const uint4 w4 = *q;
+                const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                  o[h] = pack_bf16x2(fin.keep * bf16_bits_to_float(ww[h] & 0xFFFFu) - us * bf16_bits_to_float(o[h] & 0xFFFFu),
+                                     fin.keep * bf16_bits_to_float(ww[h] >> 16) - us * bf16_bits_to_float(o[h] >> 16));
+              }
+              *q = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          } else {
+            // The transposed box: 64 rows (the box's columns) x 128 columns (the tile's rows), unswizzled.
+            uint16_t* q = reinterpret_cast<uint16_t*>(stg_box(box));
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const int idx = c * 128 + quarter * 32 + lane;
+              const uint16_t xk = static_cast<uint16_t>((c & 1) ? (pk[box][c >> 1] >> 16) : (pk[box][c >> 1] & 0xFFFFu));
+              q[idx] = fin.update ? to_bf16_bits(fin.keep * bf16_bits_to_float(q[idx]) - us * bf16_bits_to_float(xk)) : xk;
+            }
+          }
+          store_box(box, &fin.map[mi], tr ? y_tile : x0, tr ? x0 : y_tile, 0);
+        }
+      } else if (!skip) {
 #pragma unroll
         for (int box = 0; box < kBoxes; ++box) {
           float v[64];
@@ -532,53 +623,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             free_box(false);  // the store two back from this box has read it
             ++ring;
           }
-          if constexpr (kFinal) {
-            // Straight into the caller's matrix: the box at (x0, y_tile) of X_k, transposed for trans.
-            const int mi = fin.first[td.x] + td.y;
-            const bool tr = fin.trans[mi] != 0;
-            const int ux = tr ? y_tile : x0, uy = tr ? x0 : y_tile;
-            if (fin.update) {
-              fence_proxy_async_smem();  // the addend reads above come before the load's writes
-              sync_half();
-              if (leader) {
-                mbar_arrive_expect_tx(box_bar(b), 16384u);
-                tma_load_3d(smem_u32(stg_box(b)), &fin.map[mi], box_bar(b), ux, uy, 0);
-              }
-              box_pending |= 1u << b;
-              wait_box(b);
-            }
-            const float us = fin.scale[mi];
-            if (!tr) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                uint4* p = reinterpret_cast<uint4*>(row_ptr + ((j ^ (lane & 7)) * 16));
-                uint32_t ww[4] = {0u, 0u, 0u, 0u};
-                if (fin.update) {
-                  const uint4 w4 = *p;
-                  ww[0] = w4.x; ww[1] = w4.y; ww[2] = w4.z; ww[3] = w4.w;
-                }
-                uint32_t o[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                  const float lo = v[8 * j + 2 * h], hi = v[8 * j + 2 * h + 1];
-                  o[h] = fin.update ? pack_bf16x2(fin.keep * bf16_bits_to_float(ww[h] & 0xFFFFu) - us * lo,
-                                                  fin.keep * bf16_bits_to_float(ww[h] >> 16) - us * hi)
-                                    : pack_bf16x2(lo, hi);
-                }
-                *p = make_uint4(o[0], o[1], o[2], o[3]);
-              }
-            } else {
-              // 64 rows (the box's columns) x 128 columns (the tile's rows), unswizzled.
-              uint16_t* p = reinterpret_cast<uint16_t*>(stg_box(b));
-#pragma unroll
-              for (int c = 0; c < 64; ++c) {
-                const int idx = c * 128 + quarter * 32 + lane;
-                p[idx] = fin.update ? to_bf16_bits(fin.keep * bf16_bits_to_float(p[idx]) - us * v[c])
-                                    : to_bf16_bits(v[c]);
-              }
-            }
-            store_box(b, &fin.map[mi], ux, uy, 0);
-          } else {
+          {
             uint32_t packed[32];  // this thread's 64 output values of the box, as bf16 pairs
 #pragma unroll
             for (int k = 0; k < 32; ++k) packed[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
@@ -613,12 +658,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       sync_half();  // the abort flag, if raised in this tile, is seen by all four warps alike
       if (*abort_flag) break;
-      tc_fence_before();
-      if constexpr (kPair) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));  // the leader's barrier
-      } else {
-        mbar_arrive(tempty_bar(acc));
+      if (!released) {
+        tc_fence_before();
+        if constexpr (kPair) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));  // the leader's barrier
+        } else {
+          mbar_arrive(tempty_bar(acc));
+        }
       }
       if (++acc == 2) {
         acc = 0;
@@ -642,6 +689,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
     else
       tmem_dealloc(tmem_base, S::TMEM_COLS);
+  }
+  if (args.clk && threadIdx.x == 0) {
+    atomicAdd(args.clk, static_cast<unsigned long long>(clock64() - clk_start));
+    atomicAdd(args.clk + 1, static_cast<unsigned long long>(global_timer_ns() - ns_start));
   }
 }
 
