@@ -40,8 +40,7 @@ SMS = 148
 # DRAM bytes (read + write) per launch of each kernel from one ncu capture, keyed
 # by the hash of the kernel sources they were taken with. A stale hash gives null.
 NCU_TRAFFIC = {
-    "fc24e113884ea847": {"combine_ax_bx": 390.4e6, "gram_xxt": 210.3e6,  # ncu --set full, GPT-2 124M set
-                         "gram_aa": 126.5e6},  # the same set with the quintic
+    "d944c791516e7228": {"gram_xxt": 211.7e6},  # ncu --set full, GPT-2 124M set
 }
 
 KERNEL_SOURCES = ["muon_newton_schulz_09_b300/csrc/ns_gemm.cuh", "muon_newton_schulz_09_b300/csrc/elementwise.cuh",
