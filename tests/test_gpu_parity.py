@@ -274,3 +274,19 @@ def test_bounded_wait_expiry_is_reported_and_recoverable(muon):
     _, xs = inputs_for([(256, 384)], "bf16", seed=16)
     got = run_orth(muon, xs, "bf16", "f32", 5, CUBIC)
     assert rel_f(got[0], oracle.orthogonalize(xs[0], 5, CUBIC)) < TOL
+
+
+def test_profiling_counts_launches_and_reads_the_sm_clock(muon):
+    """Profiling brackets each kernel with events and has the GEMM kernels report their own SM clock."""
+    _, xs = inputs_for([(256, 384), (384, 256)], "bf16", seed=17)
+    muon.profile_read()  # drop anything recorded before
+    muon.profile(True)
+    got = run_orth(muon, xs, "bf16", "f32", 3, CUBIC)
+    muon.profile(False)
+    prof = muon.profile_read()
+    mhz = muon.profile_clock()
+    assert prof["gram_xxt"][1] == 3 and prof["combine_ax_bx"][1] == 3
+    assert prof["norm"][1] == 1 and all(ms > 0 for ms, n in prof.values() if n)
+    assert 300.0 < mhz < 3000.0, mhz
+    for g, x in zip(got, xs):
+        assert rel_f(g, oracle.orthogonalize(x, 3, CUBIC)) < TOL
