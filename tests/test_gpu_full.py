@@ -98,3 +98,37 @@ def test_illconditioned_4096x16384(muon):
     e = rel_f(host(out), want)
     print("illconditioned rel-F:", e)
     assert e < TOL
+
+
+def test_max_short_side_block_diagonal(muon):
+    """The largest square matrix the ABI takes (32768 x 32768, the Gram's side limit).
+
+    The input is zero except for four blocks on the diagonal, one of them at the far corner.
+    The Newton-Schulz iteration is a polynomial in X X^T applied to X, so a block-diagonal X stays
+    block-diagonal and each block evolves on its own, after the one global Frobenius
+    normalisation. The oracle computes each block alone from that global norm, and everything
+    outside the blocks must come out exactly zero: every tile of the 32768^2 Gram and combine
+    is computed, and the zero tiles check the tile bookkeeping at this size.
+    """
+    n = 32768
+    blocks = [(0, 256), (8256, 192), (20000, 300), (n - 256, 256)]  # (offset, size)
+    g = torch.zeros((n, n), dtype=torch.bfloat16, device="cuda")
+    host_blocks = []
+    for i, (o, k) in enumerate(blocks):
+        blk = wl.bf16_round(wl.normal((23, 0, i), (k, k)))
+        host_blocks.append(blk.astype(np.float64))
+        g[o:o + k, o:o + k] = torch.from_numpy(blk).to("cuda", torch.bfloat16)
+    out = torch.empty_like(g)
+    steps, coeffs = 5, (1.5, -0.5, 0.0)
+    muon.orthogonalize([g], [out], steps=steps, coeffs=coeffs)
+    torch.cuda.synchronize()
+    assert muon.get_error() == 0
+    norm = np.sqrt(sum(float(np.sum(b * b)) for b in host_blocks))
+    errs = []
+    for (o, k), b in zip(blocks, host_blocks):
+        want = oracle.newton_schulz(b / (norm + oracle.DEFAULT_EPS), steps, *coeffs)
+        errs.append(rel_f(host(out[o:o + k, o:o + k]), want))
+        out[o:o + k, o:o + k] = 0
+    assert max(errs) < TOL, errs
+    assert int(torch.count_nonzero(out)) == 0
+    print("32768^2 block-diagonal rel-F per block:", errs)
