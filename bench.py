@@ -99,7 +99,7 @@ def oriented(shape) -> tuple:
     return min(r, c), max(r, c)
 
 
-def kernel_work(w: wl.Workload) -> dict:
+def kernel_work(w: wl.Workload, carry: bool = False) -> dict:
     """Algorithmic work of each kernel kind per STEP: ("flops" | "bytes", amount).
 
     Gram: n(n+1)m flops per iteration (upper triangle); combine: 2 n^2 m per
@@ -108,11 +108,13 @@ def kernel_work(w: wl.Workload) -> dict:
     write; scale: u or input read + X0 write; update: O read + W read/write;
     copy: O read + out write). A kind may take several launches per step
     (one per iteration, or one per 128 matrices); throughput is the step's
-    work over the kind's summed launch time.
+    work over the kind's summed launch time. With the precise carry X0 and
+    O move a bf16 low part as well (2 more bytes per element).
     """
     gb = 4 if w.dtype == "f32" else 2
     pb = 4 if w.param_dtype == "f32" else 2
     elems = w.elements()
+    lo = 2 if carry else 0
     k = w.steps
     gram = sum(n * (n + 1) * m for n, m in map(oriented, w.shapes)) * k
     comb = sum(2 * n * n * m for n, m in map(oriented, w.shapes)) * k
@@ -120,12 +122,13 @@ def kernel_work(w: wl.Workload) -> dict:
     work = {"gram_xxt": ("flops", float(gram)), "combine_ax_bx": ("flops", float(comb)),
             "gram_aa": ("flops", float(aa))}
     if w.kind == "step":
-        work.update({"momentum_norm": ("bytes", float(elems * (gb + 4 + 4 + 2))),
+        work.update({"momentum_norm": ("bytes", float(elems * (gb + 4 + 4 + 2 + lo))),
                      "scale_orient": ("bytes", float(elems * (2 + 2))),
-                     "update": ("bytes", float(elems * (2 + 2 * pb)))})
+                     "update": ("bytes", float(elems * (2 + lo + 2 * pb)))})
     else:
-        work.update({"norm": ("bytes", float(elems * gb)), "scale_orient": ("bytes", float(elems * (gb + 2))),
-                     "copy_out": ("bytes", float(elems * (2 + 4)))})
+        work.update({"norm": ("bytes", float(elems * gb)),
+                     "scale_orient": ("bytes", float(elems * (gb + 2 + lo))),
+                     "copy_out": ("bytes", float(elems * (2 + lo + 4)))})
     return work
 
 
@@ -393,7 +396,8 @@ def run_ours(args) -> dict:
     w = workload_of(args.workload)
     dw = DeviceWorkload(w, local_rank)
     a, b, c = w.coeffs
-    muon = Muon(local_rank, steps=w.steps, a=a, b=b, c=c, eps=w.eps, scale_lr_by_shape=True)
+    carry = bool(getattr(args, "precise_carry", False))
+    muon = Muon(local_rank, steps=w.steps, a=a, b=b, c=c, eps=w.eps, scale_lr_by_shape=True, precise_carry=carry)
     stream = torch.cuda.current_stream()
     step = dw.prepared(muon, stream)
 
@@ -468,7 +472,7 @@ def run_ours(args) -> dict:
     sustained = (prof_s >= 1.0 or "sw_power_cap" in clk.get("reasons", [])
                  or (0 < device_mhz < 0.9 * clk.get("sm_max_mhz", peaks.get("sm_max_mhz", 2032.0))))
     tc_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-    work = kernel_work(w)
+    work = kernel_work(w, carry)
     kernels = {}
     for name, (ms, n) in prof.items():
         if n == 0:
@@ -510,6 +514,7 @@ def run_ours(args) -> dict:
                    "ns_steps": w.steps, "coeffs": list(w.coeffs), "kind": w.kind,
                    "parallelism": f"replicas x{world} (one full step per GPU, no collective)",
                    "l2": f"inputs larger than L2: {dw.resident_bytes() / 1e6:.0f} MB resident per step",
+                   "precise_carry": carry,
                    "alg_flops_per_step": step_flops(w)},
         "roofline": roofline,
         "gemm_tflops_per_step": round(gemm_tflops, 1) if gemm_tflops else None,
@@ -575,6 +580,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=wl.GPT2_124M.name, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--precise-carry", action="store_true", help="carry X between iterations as bf16 hi + lo")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     line = run_reference(args) if args.impl == "reference" else run_ours(args)

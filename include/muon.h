@@ -88,18 +88,28 @@ typedef struct {
  * zero applies s = 1. weight_decay (>= 0): decoupled decay, step 6 becomes
  * W <- W * (1 - lr * weight_decay) - lr * s * O. The energy-efficiency article
  * on Modded-NanoGPT (hyperparameter paragraph) reports wd = 1.0; the form is
- * this library's reading. */
+ * this library's reading.
+ * precise_carry (0 or 1): 0 rounds X to bf16 after every iteration, the stated
+ * bf16 arithmetic. 1 carries X between iterations as two bf16 parts,
+ * hi = bf16(X) and lo = bf16(X - hi). The tensor cores still take hi. The
+ * a*X term, X0 and the final O use hi + lo (about 16 significant bits), so
+ * rounding noise does not build up over the iterations. On gradients with a
+ * few dominant directions this cuts the distance to the exact iteration by
+ * one to two orders of magnitude. It costs a second pair of X buffers in
+ * the workspace, 4 more bytes per element in each combine pass, and combines
+ * that stage their two 64-column units one after the other. */
 typedef struct {
   int32_t steps;
   float a, b, c;
   float eps;
   int32_t scale_lr_by_shape;
   float weight_decay;
+  int32_t precise_carry;
 } muon_config;
 
 /* Fills *cfg with the defaults: steps 5, (a,b,c) = (1.5, -0.5, 0), eps 1e-7,
- * scale_lr_by_shape 1, weight_decay 0. The cubic coefficients are the
- * iteration's textbook form; the pages give none. */
+ * scale_lr_by_shape 1, weight_decay 0, precise_carry 0. The cubic coefficients
+ * are the iteration's textbook form; the pages give none. */
 void muon_default_config(muon_config* cfg);
 
 /* Creates a handle on CUDA device `device`. cfg may be NULL (defaults).

@@ -34,7 +34,8 @@ class MuonMatrix(ctypes.Structure):
 
 class MuonConfig(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_int32), ("a", ctypes.c_float), ("b", ctypes.c_float), ("c", ctypes.c_float),
-                ("eps", ctypes.c_float), ("scale_lr_by_shape", ctypes.c_int32), ("weight_decay", ctypes.c_float)]
+                ("eps", ctypes.c_float), ("scale_lr_by_shape", ctypes.c_int32), ("weight_decay", ctypes.c_float),
+                ("precise_carry", ctypes.c_int32)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -190,10 +191,12 @@ class Muon:
     """A libmuon handle on one CUDA device."""
 
     def __init__(self, device: int = 0, steps: int = 5, a: float = 1.5, b: float = -0.5, c: float = 0.0,
-                 eps: float = 1e-7, scale_lr_by_shape: bool = True, weight_decay: float = 0.0):
+                 eps: float = 1e-7, scale_lr_by_shape: bool = True, weight_decay: float = 0.0,
+                 precise_carry: bool = False):
         self.lib = load_library()
         self.device = device
-        self.config = MuonConfig(steps, a, b, c, eps, int(bool(scale_lr_by_shape)), weight_decay)
+        self.config = MuonConfig(steps, a, b, c, eps, int(bool(scale_lr_by_shape)), weight_decay,
+                                 int(bool(precise_carry)))
         h = ctypes.c_void_p()
         st = self.lib.muon_create(ctypes.byref(h), device, ctypes.byref(self.config))
         if st != MUON_OK:

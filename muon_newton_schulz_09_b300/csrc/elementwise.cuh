@@ -51,6 +51,29 @@ __device__ __forceinline__ void store8(void* base, int64_t idx, const float (&v)
   }
 }
 
+// x held as a pair of bf16 values (precise carry): hi = bf16(x), lo = bf16(x - hi), so that hi + lo
+// keeps about 16 significant bits of x.
+__device__ __forceinline__ uint16_t lo_part(float x, uint16_t hi) { return f_to_bf16(x - bf16_to_f(hi)); }
+
+// Stores eight values as bf16 at hi + idx and, when lo is not null, their low parts at lo + idx.
+__device__ __forceinline__ void store8_split(uint16_t* hi, uint16_t* lo, int64_t idx, const float (&v)[8]) {
+  uint32_t wh[4], wl[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const uint16_t h0 = f_to_bf16(v[2 * h]), h1 = f_to_bf16(v[2 * h + 1]);
+    wh[h] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+    wl[h] = static_cast<uint32_t>(lo_part(v[2 * h], h0)) | (static_cast<uint32_t>(lo_part(v[2 * h + 1], h1)) << 16);
+  }
+  *reinterpret_cast<uint4*>(hi + idx) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+  if (lo) *reinterpret_cast<uint4*>(lo + idx) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+}
+
+__device__ __forceinline__ void store1_split(uint16_t* hi, uint16_t* lo, int64_t idx, float v) {
+  const uint16_t h = f_to_bf16(v);
+  hi[idx] = h;
+  if (lo) lo[idx] = lo_part(v, h);
+}
+
 // Eight consecutive elements in their storage form (one or two 16-byte words), so that every
 // load of a thread can be in flight before any of them is unpacked.
 template <bool kF32>
@@ -131,6 +154,7 @@ struct MomMat {
   const void* g;       // gradient or orthogonalize input (fp32 or bf16)
   float* buf;          // momentum, fp32
   uint16_t* u;         // bf16 u in the Newton-Schulz orientation (n x m, ld_u), or nullptr (norm only)
+  uint16_t* u_lo;      // its low parts (precise carry), same layout, or nullptr
   int64_t ld_g, ld_buf, ld_u;
   int rows, cols;      // caller orientation
   int transposed;      // u = (g-side matrix)^T: written through a 128 x 64 shared-memory tile
@@ -208,7 +232,7 @@ __global__ void __launch_bounds__(kEwThreads, kSrcF32 ? 3 : 4) momentum_norm_ker
             ss += u[k] * u[k];
           }
           if (kStep) store8<true>(M.buf, e, b);
-          if (M.u) store8<false>(M.u, e, u);
+          if (M.u) store8_split(M.u, M.u_lo, e, u);
         }
       }
     } else {
@@ -218,7 +242,7 @@ __global__ void __launch_bounds__(kEwThreads, kSrcF32 ? 3 : 4) momentum_norm_ker
         float b = kStep ? M.buf[row * M.ld_buf + col] : 0.f;
         const float u = momentum_u<kStep, kSrcF32>(g, b, beta, a.nesterov);
         if (kStep) M.buf[row * M.ld_buf + col] = b;
-        if (M.u) M.u[row * M.ld_u + col] = f_to_bf16(u);
+        if (M.u) store1_split(M.u, M.u_lo, row * M.ld_u + col, u);
         ss += u * u;
       }
     }
@@ -285,11 +309,11 @@ __global__ void __launch_bounds__(kEwThreads, kSrcF32 ? 3 : 4) momentum_norm_ker
         for (int k = 0; k < 8; ++k) uv[k] = tile[dcol + k][cc];
         const int64_t di = static_cast<int64_t>(dr) * M.ld_u + dc;
         if (M.vec_ok && dc + 7 < M.rows) {
-          store8<false>(M.u, di, uv);
+          store8_split(M.u, M.u_lo, di, uv);
         } else {
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            if (dc + k < M.rows) M.u[di + k] = f_to_bf16(uv[k]);
+            if (dc + k < M.rows) store1_split(M.u, M.u_lo, di + k, uv[k]);
         }
       }
     }
@@ -343,9 +367,10 @@ __global__ void __launch_bounds__(kEwThreads, kSrcF32 ? 3 : 4) momentum_norm_ker
       const float f = inv_s;
       const int64_t n = M.transposed ? M.cols : M.rows, m = M.transposed ? M.rows : M.cols;
       for (int64_t e = threadIdx.x; e < n * m; e += kEwThreads) {
-        const int64_t row = e / m, col = e - row * m;
-        uint16_t* p = M.u + row * M.ld_u + col;
-        *p = f_to_bf16(bf16_to_f(__ldcg(p)) * f);
+        const int64_t row = e / m, col = e - row * m, i = row * M.ld_u + col;
+        float x = bf16_to_f(__ldcg(M.u + i));
+        if (M.u_lo) x += bf16_to_f(__ldcg(M.u_lo + i));
+        store1_split(M.u, M.u_lo, i, x * f);
       }
     }
   }
@@ -365,6 +390,8 @@ enum MapMode { kScale = 0, kUpdate = 1, kCopy = 2 };
 struct MapMat {
   const void* src;
   void* dst;
+  const uint16_t* src_lo;  // kUpdate / kCopy with the precise carry: low parts of src (bf16, src's layout)
+  uint16_t* dst_lo;        // kScale with the precise carry: low parts of dst (bf16, dst's layout)
   int64_t ld_src, ld_dst;
   int sr, sc;          // source rows, cols
   int transposed;
@@ -386,8 +413,27 @@ template <int kMode, bool kDstF32>
 __device__ __forceinline__ void map_apply1(const MapMat& M, float f, float s, int64_t di, float keep) {
   if (kMode == kUpdate)
     store1<kDstF32>(M.dst, di, keep * load1<kDstF32>(M.dst, di) - f * s);
+  else if (kMode == kScale && M.dst_lo)
+    store1_split(static_cast<uint16_t*>(M.dst), M.dst_lo, di, s * f);
   else
     store1<kDstF32>(M.dst, di, (kMode == kScale) ? s * f : s);
+}
+
+// The source value at si: src, plus its low part under the precise carry.
+template <bool kSrcF32>
+__device__ __forceinline__ float map_src1(const MapMat& M, int64_t si) {
+  float v = load1<kSrcF32>(M.src, si);
+  if (M.src_lo) v += bf16_to_f(M.src_lo[si]);
+  return v;
+}
+
+// Eight results at di: dst (and dst_lo for kScale under the precise carry).
+template <int kMode, bool kDstF32>
+__device__ __forceinline__ void map_store8(const MapMat& M, int64_t di, const float (&d)[8]) {
+  if (kMode == kScale && !kDstF32)
+    store8_split(static_cast<uint16_t*>(M.dst), M.dst_lo, di, d);
+  else
+    store8<kDstF32>(M.dst, di, d);
 }
 
 // d = f(s) for eight elements: the old destination values dold are used by kUpdate only.
@@ -425,11 +471,13 @@ __global__ void __launch_bounds__(kEwThreads, 3) map_kernel(const __grid_constan
       constexpr int V = kFlatChunk / (kEwThreads * 8);
       Raw8<kSrcF32> sr[V];
       Raw8<kDstF32> dr[V];
+      Raw8<false> lr[V];
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int64_t e = e0 + (static_cast<int64_t>(v) * kEwThreads + threadIdx.x) * 8;
         if (e < e1) {
           sr[v] = ld_raw8<kSrcF32>(M.src, e);
+          if (kMode != kScale && M.src_lo) lr[v] = ld_raw8<false>(M.src_lo, e);
           if (kMode == kUpdate) dr[v] = ld_raw8<kDstF32>(M.dst, e);
         }
       }
@@ -439,15 +487,21 @@ __global__ void __launch_bounds__(kEwThreads, 3) map_kernel(const __grid_constan
         if (e < e1) {
           float sv[8], dold[8], d[8];
           unpack8<kSrcF32>(sr[v], sv);
+          if (kMode != kScale && M.src_lo) {
+            float lo[8];
+            unpack8<false>(lr[v], lo);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sv[k] += lo[k];
+          }
           if (kMode == kUpdate) unpack8<kDstF32>(dr[v], dold);
           map_combine8<kMode>(f, sv, dold, d, a.keep);
-          store8<kDstF32>(M.dst, e, d);
+          map_store8<kMode, kDstF32>(M, e, d);
         }
       }
     } else {
       for (int64_t e = e0 + threadIdx.x; e < e1; e += kEwThreads) {
         const int64_t row = e / cols, col = e - row * cols;
-        map_apply1<kMode, kDstF32>(M, f, load1<kSrcF32>(M.src, row * M.ld_src + col), row * M.ld_dst + col, a.keep);
+        map_apply1<kMode, kDstF32>(M, f, map_src1<kSrcF32>(M, row * M.ld_src + col), row * M.ld_dst + col, a.keep);
       }
     }
     return;
@@ -467,10 +521,14 @@ __global__ void __launch_bounds__(kEwThreads, 3) map_kernel(const __grid_constan
   constexpr int P1 = kTileRows / 32, P2 = kTile / 16;
   Raw8<kSrcF32> sraw[P1];
   Raw8<kDstF32> draw[P2];
+  Raw8<false> lraw[P1];
 #pragma unroll
   for (int p = 0; p < P1; ++p) {
     const int gr = r0 + p * 32 + sub, gc = c0 + c8;
-    if (M.vec_ok && gr < M.sr && gc + 7 < M.sc) sraw[p] = ld_raw8<kSrcF32>(M.src, static_cast<int64_t>(gr) * M.ld_src + gc);
+    if (M.vec_ok && gr < M.sr && gc + 7 < M.sc) {
+      sraw[p] = ld_raw8<kSrcF32>(M.src, static_cast<int64_t>(gr) * M.ld_src + gc);
+      if (kMode != kScale && M.src_lo) lraw[p] = ld_raw8<false>(M.src_lo, static_cast<int64_t>(gr) * M.ld_src + gc);
+    }
   }
   if (kMode == kUpdate) {
 #pragma unroll
@@ -486,11 +544,16 @@ __global__ void __launch_bounds__(kEwThreads, 3) map_kernel(const __grid_constan
     float v[8];
     if (M.vec_ok && gr < M.sr && gc + 7 < M.sc) {
       unpack8<kSrcF32>(sraw[p], v);
+      if (kMode != kScale && M.src_lo) {
+        float lo[8];
+        unpack8<false>(lraw[p], lo);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] += lo[k];
+      }
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        v[k] = (gr < M.sr && gc + k < M.sc) ? load1<kSrcF32>(M.src, static_cast<int64_t>(gr) * M.ld_src + gc + k)
-                                            : 0.f;
+        v[k] = (gr < M.sr && gc + k < M.sc) ? map_src1<kSrcF32>(M, static_cast<int64_t>(gr) * M.ld_src + gc + k) : 0.f;
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) tile[r][c8 + k] = v[k];
@@ -509,7 +572,7 @@ __global__ void __launch_bounds__(kEwThreads, 3) map_kernel(const __grid_constan
       float dold[8], d[8];
       if (kMode == kUpdate) unpack8<kDstF32>(draw[p], dold);
       map_combine8<kMode>(f, sv, dold, d, a.keep);
-      store8<kDstF32>(M.dst, di, d);
+      map_store8<kMode, kDstF32>(M, di, d);
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k)

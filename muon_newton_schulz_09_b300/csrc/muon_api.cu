@@ -41,6 +41,8 @@ constexpr bool kPairMma = MUON_GEMM_PAIR != 0;
 constexpr int kGramBN = 256, kGramStages = kPairMma ? 5 : 3;
 constexpr int kCombBN = 256, kCombStages = kPairMma ? 5 : 3;
 constexpr int kCluster = 2;  // the two CTAs that share one B block
+// Kernel parameters are limited to 32764 bytes.
+static_assert(sizeof(GemmArgs) + sizeof(FinalArgs<kMaxFinal>) <= 32764, "GEMM parameter block too large");
 using GramShape = GemmShape<true, kGramBN, kGramStages, kPairMma>;
 using CombShape = GemmShape<false, kCombBN, kCombStages, kPairMma>;
 
@@ -142,6 +144,7 @@ struct Group {
   int first_slot = 0;  // the group's first matrix in group order
   int64_t ld_x = 0, ld_p = 0;
   size_t x_off[2] = {0, 0}, p_off = 0, a_off = 0;  // byte offsets in the workspace
+  size_t lo_off[2] = {0, 0};  // precise carry: low parts of X, laid out like X (allocated only then)
 };
 
 struct GemmBatch {           // up to kMaxGroups groups served by one launch
@@ -405,6 +408,10 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
     g.x_off[1] = take(xb);
     g.p_off = take(pb);
     g.a_off = take(pb);
+    if (h->cfg.precise_carry) {
+      g.lo_off[0] = take(xb);
+      g.lo_off[1] = take(xb);
+    }
   }
   int64_t nparts = 0;
   for (MatInfo& mi : P.mats) {
@@ -529,6 +536,12 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
         B.comb[t].grp[gi] = GemmGroup{reinterpret_cast<uint16_t*>(xb[t]), nullptr, g.n * g.ld_x, static_cast<int>(g.n),
                                       static_cast<int>(g.m), static_cast<int>(g.ld_x),
                                       static_cast<int>(ceil_div(g.n, 64))};
+        if (h->cfg.precise_carry) {  // addend and output low parts, laid out like X
+          uint8_t* lb[2] = {P.ws + g.lo_off[0], P.ws + g.lo_off[1]};
+          ok &= encode_map(h, &B.comb[t].map_e_lo[gi], lb[t], g.m, g.n, g.count, g.ld_x, 64, 128);
+          ok &= encode_map(h, &B.comb[t].map_out_lo[gi], lb[1 - t], g.m, g.n, g.count, g.ld_x, 64, 128);
+          B.comb[t].carry = 1;
+        }
       }
       // A A pass: operands are rows of A (symmetric), addend A, output B.
       ok &= encode_map(h, &B.gram_aa.map_a[gi], abuf, g.n, g.n, g.count, g.ld_p, 64, 128);
@@ -580,6 +593,13 @@ muon_status get_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t
 uint16_t* x_slot(const Plan& P, const MatInfo& mi, int t) {
   const Group& g = P.groups[mi.group];
   return reinterpret_cast<uint16_t*>(P.ws + g.x_off[t]) + static_cast<int64_t>(mi.idx) * g.n * g.ld_x;
+}
+
+// The low parts of X_t (precise carry), or nullptr.
+uint16_t* lo_slot(const Plan& P, const MatInfo& mi, int t) {
+  const Group& g = P.groups[mi.group];
+  if (g.lo_off[t] == 0) return nullptr;
+  return reinterpret_cast<uint16_t*>(P.ws + g.lo_off[t]) + static_cast<int64_t>(mi.idx) * g.n * g.ld_x;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -651,6 +671,7 @@ muon_status launch_momentum(muon_handle h, const Plan& P, const muon_matrix* src
     M.buf = kStep ? static_cast<float*>(buf[j].ptr) : nullptr;
     M.ld_buf = kStep ? buf[j].ld : 0;
     M.u = kStep ? x_slot(P, mi, 0) : nullptr;
+    M.u_lo = kStep ? lo_slot(P, mi, 0) : nullptr;
     M.ld_u = g.ld_x;
     M.rows = static_cast<int>(mi.rows);
     M.cols = static_cast<int>(mi.cols);
@@ -687,14 +708,18 @@ template <int kMode>
 muon_status launch_map_dispatch(muon_handle h, const MapArgs& a, int blocks, bool src_f32, bool dst_f32,
                                 cudaStream_t s, int kind) {
   ProfScope ps(h, kind, s);
-  if (src_f32 && dst_f32)
-    launch_pdl(map_kernel<kMode, true, true>, blocks, kEwThreads, 0, s, a);
-  else if (src_f32)
-    launch_pdl(map_kernel<kMode, true, false>, blocks, kEwThreads, 0, s, a);
-  else if (dst_f32)
-    launch_pdl(map_kernel<kMode, false, true>, blocks, kEwThreads, 0, s, a);
-  else
-    launch_pdl(map_kernel<kMode, false, false>, blocks, kEwThreads, 0, s, a);
+  // Only the scale pass reads the caller's (possibly fp32) matrices; the others read the bf16 workspace.
+  if constexpr (kMode == kScale) {
+    if (src_f32)
+      launch_pdl(map_kernel<kMode, true, false>, blocks, kEwThreads, 0, s, a);
+    else
+      launch_pdl(map_kernel<kMode, false, false>, blocks, kEwThreads, 0, s, a);
+  } else {
+    if (dst_f32)
+      launch_pdl(map_kernel<kMode, false, true>, blocks, kEwThreads, 0, s, a);
+    else
+      launch_pdl(map_kernel<kMode, false, false>, blocks, kEwThreads, 0, s, a);
+  }
   return launch_checked(h, "map kernel");
 }
 
@@ -732,6 +757,7 @@ muon_status launch_map(muon_handle h, const Plan& P, const muon_matrix* user, in
       M.ld_src = user[j].ld;
       src_f32 = user_f32;
       M.dst = x_slot(P, mi, 0);
+      M.dst_lo = lo_slot(P, mi, 0);
       M.ld_dst = g.ld_x;
       M.sr = static_cast<int>(mi.rows);
       M.sc = static_cast<int>(mi.cols);
@@ -739,6 +765,7 @@ muon_status launch_map(muon_handle h, const Plan& P, const muon_matrix* user, in
       M.inv = P.inv + j;
     } else {
       M.src = x_slot(P, mi, xk);
+      M.src_lo = lo_slot(P, mi, xk);
       M.ld_src = g.ld_x;
       M.dst = user[j].ptr;
       M.ld_dst = user[j].ld;
@@ -958,6 +985,7 @@ void muon_default_config(muon_config* cfg) {
   cfg->eps = 1e-7f;
   cfg->scale_lr_by_shape = 1;
   cfg->weight_decay = 0.0f;
+  cfg->precise_carry = 0;
 }
 
 const char* muon_status_string(muon_status s) {
@@ -1104,7 +1132,7 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
   *out = nullptr;
   if (cfg && (cfg->steps < 0 || cfg->steps > kMaxSteps || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->a) ||
               !std::isfinite(cfg->b) || !std::isfinite(cfg->c) || !(cfg->weight_decay >= 0.0f) ||
-              !std::isfinite(cfg->weight_decay)))
+              !std::isfinite(cfg->weight_decay) || (cfg->precise_carry != 0 && cfg->precise_carry != 1)))
     return MUON_ERR_INVALID;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) {

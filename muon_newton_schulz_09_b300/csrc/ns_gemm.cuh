@@ -54,6 +54,9 @@ struct GemmArgs {
   CUtensorMap map_out[kMaxGroups];     // output, box 64 columns x 128 rows, 128-byte swizzle
   CUtensorMap map_mirror[kMaxGroups];  // Gram output again, box 128 columns x 64 rows, no swizzle
   CUtensorMap map_e[kMaxGroups];       // addend E, box 64 columns x 128 rows, 128-byte swizzle
+  // Combine under the precise carry: the low parts of E and of the output, same boxes.
+  CUtensorMap map_e_lo[kMaxGroups];
+  CUtensorMap map_out_lo[kMaxGroups];
   GemmGroup grp[kMaxGroups];
   const int4* tiles;              // {group, matrix within group, tile row, tile col}
   const int* cta_begin;           // CTA b walks tiles[cta_begin[b] .. cta_begin[b+1])
@@ -64,6 +67,7 @@ struct GemmArgs {
   float s_e;
   int* err;
   unsigned long long* clk;  // non-null while profiling: += {SM cycles, ns} of every CTA of the launch
+  int carry;                // combine: X is carried as hi + lo (E and the output each in two bf16 parts)
 };
 
 // The last combine of a call can write its result straight into the caller's
@@ -472,6 +476,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int ring = 0;  // Gram: staging boxes are used in turn by every store
+    const bool carry = !kGram && args.carry != 0;
+    // Precise carry: box 0 holds the high part and box 1 the low part of unit u's addend. v gets
+    // s_e * (hi + lo) added, and the two boxes then take the output's high and low parts in place.
+    auto add_carried_addend = [&](float (&v)[64], float s_e_) {
+      wait_box(0);
+      wait_box(1);
+      const uint8_t* rh = stg_box(0) + (quarter * 32 + lane) * 128;
+      const uint8_t* rl = stg_box(1) + (quarter * 32 + lane) * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 h4 = *reinterpret_cast<const uint4*>(rh + ((j ^ (lane & 7)) * 16));
+        const uint4 l4 = *reinterpret_cast<const uint4*>(rl + ((j ^ (lane & 7)) * 16));
+        const uint32_t hh[4] = {h4.x, h4.y, h4.z, h4.w}, ll[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          v[8 * j + 2 * h] += s_e_ * (bf16_bits_to_float(hh[h] & 0xFFFFu) + bf16_bits_to_float(ll[h] & 0xFFFFu));
+          v[8 * j + 2 * h + 1] += s_e_ * (bf16_bits_to_float(hh[h] >> 16) + bf16_bits_to_float(ll[h] >> 16));
+        }
+      }
+    };
     for (int t = t_begin; t < t_end; ++t) {
       const int4 td = args.tiles[t];
       const int I = td.z + rank;
@@ -492,9 +516,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const float s_e = args.s_e * (kGram ? 1.0f : post);
       // Addend boxes (box b of this tile through staging box b): box 0 may reuse its staging box
       // once all but the latest store have read theirs, box 1 once all have.
+      // Under the precise carry the two boxes hold the high and low parts of one unit's addend,
+      // and both wait until every store has read its box.
       if (has_e && !skip) {
-        load_box(0, &args.map_e[td.x], col_base, y_tile, td.y, false);
-        load_box(1, &args.map_e[td.x], col_base + 64, y_tile, td.y, true);
+        if (carry) {
+          load_box(0, &args.map_e[td.x], col_base, y_tile, td.y, true);
+          load_box(1, &args.map_e_lo[td.x], col_base, y_tile, td.y, true);
+        } else {
+          load_box(0, &args.map_e[td.x], col_base, y_tile, td.y, false);
+          load_box(1, &args.map_e[td.x], col_base + 64, y_tile, td.y, true);
+        }
       }
       // A wait that gives up (and raises the CTA abort flag) does not leave the loop on its own:
       // every warp of the half goes through the same barriers, and all four leave together after
@@ -502,7 +533,91 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err);
       tc_fence_after();
       bool released = false;  // the accumulator has been handed back to the MMA warp
-      if constexpr (kFinal) {
+      if (carry && !skip) {
+        // Precise carry: the two units of the half run one after the other through both boxes.
+#pragma unroll 1
+        for (int box = 0; box < kBoxes; ++box) {
+          const int x0 = col_base + box * 64;
+          if (box == 1) {  // unit 1's addend parts, once every store has read its box
+            load_box(0, &args.map_e[td.x], x0, y_tile, td.y, true);
+            load_box(1, &args.map_e_lo[td.x], x0, y_tile, td.y, true);
+          }
+          float v[64];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t r[32];
+            tmem_load_32cols(
+                tmem_base + lane_field + static_cast<uint32_t>(acc * kBN + half * kHalfCols + box * 64 + cc * 32), r);
+            tmem_load_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[cc * 32 + k] = s_acc * __uint_as_float(r[k]);
+          }
+          add_carried_addend(v, s_e);
+          uint8_t* rh = stg_box(0) + (quarter * 32 + lane) * 128;
+          uint8_t* rl = stg_box(1) + (quarter * 32 + lane) * 128;
+          if constexpr (kFinal) {
+            // X_k = v exactly as carried: W' = keep * W - scale * X_k, or out = bf16(X_k), through box 0.
+            const int mi = fin.first[td.x] + td.y;
+            const bool tr = fin.trans[mi] != 0;
+            const float us = fin.scale[mi];
+            const int ux = tr ? y_tile : x0, uy = tr ? x0 : y_tile;
+            if (fin.update) {
+              fence_proxy_async_smem();  // the addend reads above come before the load's writes
+              sync_half();
+              if (leader) {
+                mbar_arrive_expect_tx(box_bar(0), 16384u);
+                tma_load_3d(smem_u32(stg_box(0)), &fin.map[mi], box_bar(0), ux, uy, 0);
+              }
+              box_pending |= 1u;
+              wait_box(0);
+            }
+            if (!tr) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint4* q = reinterpret_cast<uint4*>(rh + ((j ^ (lane & 7)) * 16));
+                uint32_t ww[4] = {0u, 0u, 0u, 0u};
+                if (fin.update) {
+                  const uint4 w4 = *q;
+                  ww[0] = w4.x; ww[1] = w4.y; ww[2] = w4.z; ww[3] = w4.w;
+                }
+                uint32_t o[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                  const float x0v = v[8 * j + 2 * h], x1v = v[8 * j + 2 * h + 1];
+                  o[h] = fin.update ? pack_bf16x2(fin.keep * bf16_bits_to_float(ww[h] & 0xFFFFu) - us * x0v,
+                                                  fin.keep * bf16_bits_to_float(ww[h] >> 16) - us * x1v)
+                                    : pack_bf16x2(x0v, x1v);
+                }
+                *q = make_uint4(o[0], o[1], o[2], o[3]);
+              }
+            } else {
+              uint16_t* q = reinterpret_cast<uint16_t*>(stg_box(0));
+#pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                const int idx = c * 128 + quarter * 32 + lane;
+                q[idx] = fin.update ? to_bf16_bits(fin.keep * bf16_bits_to_float(q[idx]) - us * v[c]) : to_bf16_bits(v[c]);
+              }
+            }
+            store_box(0, &fin.map[mi], ux, uy, 0);
+          } else {
+            // The output's high and low parts, in place of the addend's (each thread rewrites its own row).
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint32_t oh[4], ol[4];
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const float x0v = v[8 * j + 2 * h], x1v = v[8 * j + 2 * h + 1];
+                oh[h] = pack_bf16x2(x0v, x1v);
+                ol[h] = pack_bf16x2(x0v - bf16_bits_to_float(oh[h] & 0xFFFFu), x1v - bf16_bits_to_float(oh[h] >> 16));
+              }
+              *reinterpret_cast<uint4*>(rh + ((j ^ (lane & 7)) * 16)) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+              *reinterpret_cast<uint4*>(rl + ((j ^ (lane & 7)) * 16)) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+            }
+            store_box(0, &args.map_out[td.x], x0, y_tile, td.y);
+            store_box(1, &args.map_out_lo[td.x], x0, y_tile, td.y);
+          }
+        }
+      } else if constexpr (kFinal) {
         // The last combine writes straight into the caller's matrices. Both boxes of X_k are first
         // taken into registers as bf16 (the value the workspace would have held), the accumulator
         // is released at once, and only then are the caller's two boxes loaded in place of the

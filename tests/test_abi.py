@@ -26,7 +26,8 @@ def test_status_strings_and_kernel_names():
 def test_default_config():
     cfg = mu.MuonConfig()
     mu.load_library().muon_default_config(ctypes.byref(cfg))
-    assert (cfg.steps, cfg.a, cfg.b, cfg.c, cfg.scale_lr_by_shape, cfg.weight_decay) == (5, 1.5, -0.5, 0.0, 1, 0.0)
+    assert (cfg.steps, cfg.a, cfg.b, cfg.c, cfg.scale_lr_by_shape, cfg.weight_decay, cfg.precise_carry) == (
+        5, 1.5, -0.5, 0.0, 1, 0.0, 0)
     assert abs(cfg.eps - 1e-7) < 1e-12
 
 

@@ -290,3 +290,89 @@ def test_profiling_counts_launches_and_reads_the_sm_clock(muon):
     assert 300.0 < mhz < 3000.0, mhz
     for g, x in zip(got, xs):
         assert rel_f(g, oracle.orthogonalize(x, 3, CUBIC)) < TOL
+
+
+# ---------------------------------------------------------------- precise carry (X as bf16 hi + lo)
+
+@pytest.fixture(scope="module")
+def muon_carry():
+    from muon_newton_schulz_09_b300 import Muon
+    with Muon(0, precise_carry=True) as m:
+        yield m
+
+
+def spiked_inputs(shapes, seed):
+    """N(0, 1e-3) plus a rank-4 spike 50x as strong: the bulk singular values sit far below the spike's."""
+    w = wl.small_workload("spk", shapes, dtype="bf16", grad_std=1e-3, spike_rank=4, spike_gain=50.0, seed=seed)
+    return [wl.gradient(w, j) for j in range(w.count)]
+
+
+@pytest.mark.parametrize("coeffs,steps,out_dtype", [(CUBIC, 5, "f32"), (QUINTIC, 5, "f32"), (QUINTIC, 3, "bf16")],
+                         ids=["cubic5_f32", "quintic5_f32", "quintic3_bf16"])
+def test_precise_carry_orthogonalize(muon, muon_carry, coeffs, steps, out_dtype):
+    """With the carry every ragged, transposed and square matrix is within the bar, and for fp32
+    outputs at least four times closer to the oracle than with X rounded to bf16 every iteration."""
+    shapes = [(128, 256), (256, 128), (130, 70), (70, 130), (384, 96), (300, 300), (513, 1000)]
+    xs = spiked_inputs(shapes, seed=41)
+    got_c = run_orth(muon_carry, xs, "bf16", out_dtype, steps, coeffs)
+    got = run_orth(muon, xs, "bf16", out_dtype, steps, coeffs)
+    for x, gc, g in zip(xs, got_c, got):
+        want = oracle.orthogonalize(x, steps, coeffs)
+        ec, e = rel_f(gc, want), rel_f(g, want)
+        assert ec < TOL, (x.shape, ec)
+        if out_dtype == "f32":
+            assert ec < 0.25 * e, (x.shape, ec, e)
+
+
+def test_precise_carry_zero_iterations_keeps_x0():
+    """steps = 0 with fp32 output: O = X0 = g/(||g||+eps) through hi + lo, far inside one bf16 rounding."""
+    from muon_newton_schulz_09_b300 import Muon
+    shapes = [(130, 70), (70, 130), (256, 256)]
+    _, xs = inputs_for(shapes, "f32", seed=42)
+    with Muon(0, precise_carry=True) as mc:
+        got = run_orth(mc, xs, "f32", "f32", 0, CUBIC)
+    for x, o in zip(xs, got):
+        assert rel_f(o, oracle.frobenius_normalize(x)) < 2e-5
+
+
+@pytest.mark.parametrize("param_dtype", ["f32", "bf16"], ids=["kernel_update", "fused_update"])
+def test_precise_carry_step(muon_carry, param_dtype):
+    """muon_step with the carry on spiked gradients: the fused last combine (bf16 params) and the update
+    kernel (fp32 params) both use X_k = hi + lo; O read back from fp32 params at zero is within 5e-3."""
+    shapes = [(256, 768), (768, 256), (130, 70), (384, 384)]
+    g = spiked_inputs(shapes, seed=43)
+    w, _, m, p = step_case(shapes, "bf16", param_dtype, seed=43)
+    lr = 0.02
+    if param_dtype == "f32":
+        P = [torch.zeros(s, device="cuda") for s in shapes]
+        p = [np.zeros(s) for s in shapes]
+    else:
+        P = [dev(x, "bf16") for x in p]
+    M = [dev(x, "f32") for x in m]
+    muon_carry.step(P, [dev(x, "bf16") for x in g], M, lr=lr, beta=0.95, nesterov=True)
+    torch.cuda.synchronize()
+    assert muon_carry.get_error() == 0
+    for j, (r, c) in enumerate(shapes):
+        w_new, buf_new, o = oracle.muon_step(p[j], g[j], m[j], lr, 0.95, True, 5, CUBIC)
+        assert rel_f(host(M[j]), buf_new) < 1e-6
+        if param_dtype == "f32":
+            assert rel_f(-host(P[j]) / (lr * oracle.lr_scale(r, c)), o) < 5e-3, (r, c)
+        else:
+            upd = lr * oracle.lr_scale(r, c) * np.abs(o).max()
+            err = np.abs(host(P[j]) - w_new)
+            assert np.all(err <= bf16_ulp(w_new) + 0.02 * upd), (r, c, float(err.max()))
+
+
+def test_precise_carry_extreme_scale(muon_carry):
+    """A norm outside the fold range: the momentum kernel rescales hi + lo in place."""
+    shapes = [(256, 512), (512, 256)]
+    g = [wl.bf16_round((x.astype(np.float64) * 1e12).astype(np.float32)) for x in spiked_inputs(shapes, seed=44)]
+    lr = 0.02
+    P = [torch.zeros(sh, device="cuda") for sh in shapes]
+    M = [torch.zeros(sh, device="cuda") for sh in shapes]
+    muon_carry.step(P, [dev(x, "bf16") for x in g], M, lr=lr, beta=0.95, nesterov=True)
+    torch.cuda.synchronize()
+    assert muon_carry.get_error() == 0
+    for j, (r, c) in enumerate(shapes):
+        _, _, o = oracle.muon_step(np.zeros((r, c)), g[j], np.zeros((r, c)), lr, 0.95, True, 5, CUBIC)
+        assert rel_f(-host(P[j]) / (lr * oracle.lr_scale(r, c)), o) < 5e-3, (r, c)
