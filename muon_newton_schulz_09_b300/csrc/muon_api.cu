@@ -589,13 +589,13 @@ muon_status get_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t
   return s;
 }
 
-// Plan for the GEMM of a batch: where X_t lives for group gi.
+// Where matrix mi's X_t (t = 0, 1: the ping-pong pair) lives in the workspace.
 uint16_t* x_slot(const Plan& P, const MatInfo& mi, int t) {
   const Group& g = P.groups[mi.group];
   return reinterpret_cast<uint16_t*>(P.ws + g.x_off[t]) + static_cast<int64_t>(mi.idx) * g.n * g.ld_x;
 }
 
-// The low parts of X_t (precise carry), or nullptr.
+// Where matrix mi's low parts of X_t live (precise carry), or nullptr without the carry.
 uint16_t* lo_slot(const Plan& P, const MatInfo& mi, int t) {
   const Group& g = P.groups[mi.group];
   if (g.lo_off[t] == 0) return nullptr;
@@ -631,7 +631,6 @@ muon_status launch_checked(muon_handle h, const char* what) {
   return MUON_OK;
 }
 
-// Norm pass (kStep = false: u = input) or momentum + norm (kStep = true).
 // Norm pass (kStep = false: u = input, nothing written) or momentum + norm (kStep = true:
 // u written in the Newton-Schulz orientation into the first X buffer, unscaled; the scale is
 // folded into the first iteration, or applied in place by the kernel for norms outside the fold range).

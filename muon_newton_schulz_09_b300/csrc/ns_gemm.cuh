@@ -100,55 +100,6 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float x) {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
-// v[0..31] += s * e[0..limit), e a bf16 row segment (16-byte aligned when limit >= 32).
-__device__ __forceinline__ void add_row32(float (&v)[32], const uint16_t* e, int limit, float s) {
-  if (limit >= 32) {
-    const uint4* p = reinterpret_cast<const uint4*>(e);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 w = p[q];
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        v[q * 8 + 2 * h] += s * bf16_bits_to_float(ww[h] & 0xFFFFu);
-        v[q * 8 + 2 * h + 1] += s * bf16_bits_to_float(ww[h] >> 16);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-      if (k < limit) v[k] += s * bf16_bits_to_float(e[k]);
-  }
-}
-
-// v[0..31] += s * (32 bf16 values held in four 16-byte registers).
-__device__ __forceinline__ void add_regs32(float (&v)[32], const uint4 (&w4)[4], float s) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t ww[4] = {w4[q].x, w4[q].y, w4[q].z, w4[q].w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      v[q * 8 + 2 * h] += s * bf16_bits_to_float(ww[h] & 0xFFFFu);
-      v[q * 8 + 2 * h + 1] += s * bf16_bits_to_float(ww[h] >> 16);
-    }
-  }
-}
-
-__device__ __forceinline__ void store_row32(uint16_t* o, const float (&v)[32], int limit) {
-  if (limit >= 32) {
-    uint4* p = reinterpret_cast<uint4*>(o);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      p[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
-                        pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-      if (k < limit) o[k] = to_bf16_bits(v[k]);
-  }
-}
-
 // Waits that must not be cut short by the abort flag: used only to let copies
 // and MMAs already in flight land before the CTA releases its resources.
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
