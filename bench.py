@@ -41,8 +41,8 @@ SMS = 148
 # by the hash of the kernel sources they were taken with. A stale hash gives null.
 NCU_TRAFFIC = {
     # ncu --set full on the GPT-2 124M set (the A A pass on its quintic variant). The combine kind
-    # averages its launches, so its figure is (4 x 389.3 MB + 556.6 MB for the last, fused one) / 5.
-    "d944c791516e7228": {"gram_xxt": 211.7e6, "combine_ax_bx": 422.8e6, "gram_aa": 127.4e6},
+    # averages its launches, so its figure is (4 x 389.4 MB + 556.5 MB for the last, fused one) / 5.
+    "711517eb4c04117e": {"gram_xxt": 211.3e6, "combine_ax_bx": 422.8e6, "gram_aa": 127.3e6},
 }
 
 KERNEL_SOURCES = ["muon_newton_schulz_09_b300/csrc/ns_gemm.cuh", "muon_newton_schulz_09_b300/csrc/elementwise.cuh",

@@ -376,3 +376,23 @@ def test_precise_carry_extreme_scale(muon_carry):
     for j, (r, c) in enumerate(shapes):
         _, _, o = oracle.muon_step(np.zeros((r, c)), g[j], np.zeros((r, c)), lr, 0.95, True, 5, CUBIC)
         assert rel_f(-host(P[j]) / (lr * oracle.lr_scale(r, c)), o) < 5e-3, (r, c)
+
+
+def test_step_more_matrices_than_one_launch_table(muon):
+    """200 bf16 matrices: the elementwise kernels split at 128 matrices per launch, and with more than
+    160 matrices in one GEMM batch the update leaves the last combine for the separate update kernel."""
+    shapes = [(64, 96)] * 120 + [(96, 64)] * 60 + [(130, 70)] * 20
+    w, g, m, p = step_case(shapes, "bf16", "bf16", seed=45)
+    lr = 0.02
+    P = [dev(x, "bf16") for x in p]
+    M = [dev(x, "f32") for x in m]
+    muon.step(P, [dev(x, "bf16") for x in g], M, lr=lr, beta=0.95, nesterov=True)
+    torch.cuda.synchronize()
+    assert muon.get_error() == 0
+    for j in (0, 119, 120, 150, 179, 180, 199):
+        r, c = shapes[j]
+        w_new, buf_new, o = oracle.muon_step(p[j], g[j], m[j], lr, 0.95, True, 5, CUBIC)
+        assert rel_f(host(M[j]), buf_new) < 1e-6
+        upd = lr * oracle.lr_scale(r, c) * np.abs(o).max()
+        err = np.abs(host(P[j]) - w_new)
+        assert np.all(err <= bf16_ulp(w_new) + 0.05 * upd), (j, float(err.max()))
