@@ -22,6 +22,16 @@ def test_kernel_work_matches_plan_stats():
     assert work["update"] == ("bytes", 84934656 * 6.0)
 
 
+def test_kernel_work_counts_the_carried_low_part():
+    w = wl.GPT2_124M
+    plain, carry = bench.kernel_work(w), bench.kernel_work(w, carry=True)
+    assert carry["momentum_norm"] == ("bytes", 84934656 * 14.0)
+    assert carry["update"] == ("bytes", 84934656 * 8.0)
+    assert carry["gram_xxt"] == plain["gram_xxt"] and carry["combine_ax_bx"] == plain["combine_ax_bx"]
+    sq = bench.kernel_work(wl.SQUARE_64x1024, carry=True)
+    assert sq["scale_orient"] == ("bytes", 64 * 1024 * 1024 * 6.0) and sq["copy_out"] == ("bytes", 64 * 1024 * 1024 * 8.0)
+
+
 def test_matrix_fraction_sums_to_one():
     for w in wl.WORKLOADS.values():
         f = bench.matrix_fraction(w)
