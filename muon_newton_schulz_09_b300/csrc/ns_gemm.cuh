@@ -17,16 +17,22 @@
 //   Combine  (kGram = false): out = s_acc * (B X) + s_e * E with B K-major
 //            (n x n) and X MN-major (n x m, row-major): E = X, s_e = a gives
 //            X' = a X + B X with the combination done on the fp32
-//            accumulator before the single bf16 rounding.
+//            accumulator before the single bf16 rounding. Under the precise
+//            carry E and X' are each a pair of bf16 parts (hi + lo); the last
+//            combine can write the caller's matrices directly (FinalArgs).
 //
-// Structure: a persistent grid (one CTA per SM, in clusters of two that share
-// the B operand through TMA multicast) walks a host-built tile list
-// covering every matrix of every shape group in the batch. Warp 0 issues TMA
-// loads into a ring of shared-memory stages, one thread of warp 1 issues
-// tcgen05.mma into a double-buffered fp32 accumulator in tensor memory, and
-// warps 2-9 drain the accumulator (tcgen05.ld), apply the epilogue and store
-// bf16 to global memory. A host-built schedule gives each CTA its own list of
-// tiles, balanced by contraction length. Every wait is bounded (see mbar_wait_bounded).
+// Structure: a persistent grid of 2-CTA clusters (one CTA per SM) walks a
+// host-built tile list covering every matrix of every shape group in the
+// batch. By default the pair runs paired-SM MMAs (tcgen05 cta_group::2,
+// M = 256): each CTA owns 128 rows of a 256 x 256 output tile and loads its
+// own A rows and half of B; built with kPair = false, each CTA runs M = 128
+// MMAs and the two share B through TMA multicast. Warp 0 issues TMA loads into
+// a ring of shared-memory stages, one thread of warp 1 (of the even CTA when
+// paired) issues tcgen05.mma into a double-buffered fp32 accumulator in
+// tensor memory, and warps 2-9 drain the accumulator (tcgen05.ld), apply the
+// epilogue and store bf16 to global memory by TMA. A host-built schedule gives
+// each cluster its own list of tiles, balanced by contraction length. Every
+// wait is bounded (see mbar_wait_bounded).
 #pragma once
 
 #include <cuda_bf16.h>
