@@ -115,3 +115,21 @@ def test_plan_stats_ragged_and_c():
 def test_selftest_wait_rejects_bad_limits_without_a_handle():
     lib = mu.load_library()
     assert lib.muon_selftest_wait(None, 50_000_000, None) == MUON_ERR_INVALID
+
+
+def test_profiling_calls_reject_a_null_handle():
+    lib = mu.load_library()
+    mhz = ctypes.c_double(-1.0)
+    assert lib.muon_profile_clock(None, ctypes.byref(mhz)) == MUON_ERR_INVALID
+    assert lib.muon_profile_enable(None, 1) == MUON_ERR_INVALID
+    assert lib.muon_profile_read(None, None, None) == MUON_ERR_INVALID
+
+
+def test_create_rejects_a_bad_config_before_touching_a_gpu():
+    lib = mu.load_library()
+    h = ctypes.c_void_p()
+    for field, value in [("precise_carry", 2), ("steps", -1), ("weight_decay", -0.5), ("eps", float("nan"))]:
+        cfg = mu.MuonConfig()
+        lib.muon_default_config(ctypes.byref(cfg))
+        setattr(cfg, field, value)
+        assert lib.muon_create(ctypes.byref(h), 0, ctypes.byref(cfg)) == MUON_ERR_INVALID, field
