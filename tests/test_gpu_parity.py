@@ -396,3 +396,22 @@ def test_step_more_matrices_than_one_launch_table(muon):
         upd = lr * oracle.lr_scale(r, c) * np.abs(o).max()
         err = np.abs(host(P[j]) - w_new)
         assert np.all(err <= bf16_ulp(w_new) + 0.05 * upd), (j, float(err.max()))
+
+
+def test_many_iterations_reach_the_polar_factor(muon):
+    """25 cubic iterations on well-conditioned inputs: the GPU result is within the bar of the fp64 iterate,
+    and both are within 2e-2 of the SVD polar factor U V^T."""
+    shapes = [(128, 384), (384, 128), (256, 256)]
+    _, xs = inputs_for(shapes, "f32", seed=46)
+    # a well-conditioned spectrum: sigma in [0.5, 1] (the iteration needs about log(1/sigma_min) steps)
+    ys = []
+    for x in xs:
+        u, s, vt = np.linalg.svd(x.astype(np.float64), full_matrices=False)
+        s = np.linspace(0.5, 1.0, s.size)[::-1]
+        ys.append(((u * s) @ vt).astype(np.float32))
+    got = run_orth(muon, ys, "f32", "f32", 25, CUBIC)
+    for y, gk in zip(ys, got):
+        want = oracle.orthogonalize(y, 25, CUBIC)
+        u, _, vt = np.linalg.svd(y.astype(np.float64), full_matrices=False)
+        assert rel_f(gk, want) < TOL
+        assert rel_f(gk, u @ vt) < 2e-2
