@@ -148,7 +148,35 @@ def step_flops(w: wl.Workload) -> float:
     return float(per * w.steps)
 
 
+def resident_bytes(w: wl.Workload) -> int:
+    """Bytes of the caller's tensors one step reads or writes: grads, momentum and params (step),
+    or inputs and bf16 outputs (orthogonalize)."""
+    gb = 4 if w.dtype == "f32" else 2
+    pb = 4 if w.param_dtype == "f32" else 2
+    per = gb + 4 + pb if w.kind == "step" else gb + 2
+    return w.elements() * per
+
+
+def config_of(w: wl.Workload, world: int, carry: bool) -> dict:
+    """The workload's description, identical for both arms."""
+    return {"workload": w.name, "description": w.notes, "matrices": w.count,
+            "ns_steps": w.steps, "coeffs": list(w.coeffs), "kind": w.kind,
+            "parallelism": f"replicas x{world} (one full step per GPU, no collective)",
+            "l2": f"inputs larger than L2: {resident_bytes(w) / 1e6:.0f} MB resident per step",
+            "precise_carry": carry,
+            "alg_flops_per_step": step_flops(w)}
+
+
 # ----------------------------------------------------------------------------- peaks and clocks
+
+# A region shorter than this is timed against the burst tensor peak (a kernel timed alone); a
+# longer one against the sustained peak measured over seconds under the power limit.
+SUSTAINED_REGION_S = 1.0
+
+
+def uses_sustained_peak(region_s: float) -> bool:
+    return region_s >= SUSTAINED_REGION_S
+
 
 def load_peaks() -> tuple:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -476,11 +504,9 @@ def run_ours(args) -> dict:
 
     # ---- roofline of the dominant kernel, from the per-kernel events of the timed region
     peaks, peak_src = load_peaks()
-    # The sustained tensor peak applies when the region ran long or under the power cap.
     clk = clk.summary()
     clk["sm_mhz_device"] = round(device_mhz, 1)
-    sustained = (prof_s >= 1.0 or "sw_power_cap" in clk.get("reasons", [])
-                 or (0 < device_mhz < 0.9 * clk.get("sm_max_mhz", peaks.get("sm_max_mhz", 2032.0))))
+    sustained = uses_sustained_peak(prof_s)
     tc_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
     work = kernel_work(w, carry)
     kernels = {}
@@ -494,7 +520,8 @@ def run_ours(args) -> dict:
             ach = amount / (avg_ms * 1e-3) / 1e12
             kernels[name] = {"launches": n, "avg_us": avg_ms * 1e3, "share": 0.0, "bound": "tensor",
                              "achieved": ach, "unit": "TFLOP/s", "frac": ach / tc_peak,
-                             "frac_burst": ach / peaks["bf16_tflops"]}
+                             "frac_burst": ach / peaks["bf16_tflops"],
+                             "frac_sustained": ach / peaks["bf16_tflops_sustained"]}
             if device_mhz > 0:  # of the dense rate at the clock the kernels ran at
                 kernels[name]["frac_per_cycle"] = ach / (DENSE_FLOPS_PER_SM_CYCLE * SMS * device_mhz * 1e6 / 1e12)
         else:
@@ -511,6 +538,10 @@ def run_ours(args) -> dict:
                 "peak": tc_peak if k["bound"] == "tensor" else peaks["hbm_gbs"], "unit": k["unit"],
                 "frac": round(k["frac"], 4), "traffic": traffic,
                 "peak_source": f"{peak_src} ({'sustained' if sustained and k['bound'] == 'tensor' else 'burst'})"}
+    if k["bound"] == "tensor":
+        roofline["frac_sustained"] = round(k["frac_sustained"], 4)
+        if "frac_per_cycle" in k:
+            roofline["frac_per_cycle"] = round(k["frac_per_cycle"], 4)
     gpu_launches = int(sum(n for ms, n in prof.values()))
     gemm_ms = sum(prof[n][0] for n in ("gram_xxt", "gram_aa", "combine_ax_bx"))
     gemm_tflops = step_flops(w) * args.steps / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
@@ -520,12 +551,7 @@ def run_ours(args) -> dict:
         "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded generators; random-init weights, no dataset)",
-        "config": {"workload": w.name, "description": w.notes, "matrices": w.count,
-                   "ns_steps": w.steps, "coeffs": list(w.coeffs), "kind": w.kind,
-                   "parallelism": f"replicas x{world} (one full step per GPU, no collective)",
-                   "l2": f"inputs larger than L2: {dw.resident_bytes() / 1e6:.0f} MB resident per step",
-                   "precise_carry": carry,
-                   "alg_flops_per_step": step_flops(w)},
+        "config": config_of(w, world, carry),
         "roofline": roofline,
         "gemm_tflops_per_step": round(gemm_tflops, 1) if gemm_tflops else None,
         "kernels": {n: {kk: (round(v, 4) if isinstance(v, float) else v) for kk, v in d.items()}
@@ -573,8 +599,7 @@ def run_reference(args) -> dict:
     return {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generators)",
-            "config": {"workload": w.name, "description": w.notes, "matrices": w.count, "ns_steps": w.steps,
-                       "coeffs": list(w.coeffs), "kind": w.kind},
+            "config": config_of(w, world, bool(getattr(args, "precise_carry", False))),
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},

@@ -171,6 +171,17 @@ muon_status muon_plan_stats(const int64_t* rows, const int64_t* cols, int count,
                             int* groups, int64_t* gram_tiles, int64_t* combine_tiles,
                             double* flops_per_iter);
 
+/* Device-memory cap for the handle's plans (workspaces and tile schedules),
+ * in bytes; 0 removes the cap (the default). A call that needs a new plan
+ * which would take the plans past the cap fails with MUON_ERR_NOMEM, exactly
+ * as it does when cudaMalloc runs out of device memory: before anything is
+ * launched, with the caller's tensors untouched and the plans already built
+ * kept. A later call (with a higher cap, or after memory is freed) builds the
+ * plan normally. bytes < 0 or h == NULL gives MUON_ERR_INVALID.
+ * muon_workspace_bytes writes the device memory the plans hold now. */
+muon_status muon_set_workspace_limit(muon_handle h, int64_t bytes);
+muon_status muon_workspace_bytes(muon_handle h, int64_t* bytes);
+
 /* Failure-detection self-test. Launches one kernel on `stream` that waits,
  * through the same bounded wait the GEMM kernels use, on a barrier that
  * nothing ever arrives at. After limit_ns (1e6 .. 2e9 ns, else
@@ -220,7 +231,10 @@ muon_status muon_profile_clock(muon_handle h, double* sm_mhz);
  * MUON_ERR_INVALID with the reason in msg, and launches nothing.
  *
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress). Make that first call before any stream capture.
+ * (cudaGetSymbolAddress), and so does the first call after the device's
+ * context has been created again (cudaDeviceReset). Make that first call
+ * before any stream capture. A device index of 64 or more returns
+ * MUON_ERR_UNSUPPORTED.
  * All calls share the one array: calls that overlap on the GPU (different
  * streams without ordering, or several host threads) race and give wrong
  * results. The tickets are cleared by every call; the other contents are left

@@ -78,6 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "muon_profile_clock": (c.c_int, [c.c_void_p, P(c.c_double)]),
         "muon_kernel_name": (c.c_char_p, [c.c_int]),
         "muon_selftest_wait": (c.c_int, [c.c_void_p, c.c_int64, c.c_void_p]),
+        "muon_set_workspace_limit": (c.c_int, [c.c_void_p, c.c_int64]),
+        "muon_workspace_bytes": (c.c_int, [c.c_void_p, P(c.c_int64)]),
         "muon_normalize_noalloc": (c.c_int, [P(MuonMatrix), P(MuonMatrix), c.c_int, c.c_float, c.c_void_p,
                                              c.c_char_p, c.c_int]),
     }
@@ -260,6 +262,16 @@ class Muon:
         """Queues the failure-detection self-test (a bounded wait that must expire)."""
         self._check(self.lib.muon_selftest_wait(self.handle, int(limit_ns), _stream_ptr(stream, self.device)),
                     "muon_selftest_wait")
+
+    def set_workspace_limit(self, nbytes: int):
+        """Caps the device memory of this handle's plans (0: no cap); see muon_set_workspace_limit."""
+        self._check(self.lib.muon_set_workspace_limit(self.handle, int(nbytes)), "muon_set_workspace_limit")
+
+    def workspace_bytes(self) -> int:
+        """Device memory the handle's plans hold now."""
+        v = ctypes.c_int64()
+        self._check(self.lib.muon_workspace_bytes(self.handle, ctypes.byref(v)), "muon_workspace_bytes")
+        return v.value
 
     def get_error(self, stream=None) -> int:
         return self.lib.muon_get_error(self.handle, _stream_ptr(stream, self.device))

@@ -32,19 +32,14 @@ using namespace muon;
 
 namespace {
 
-#ifndef MUON_GEMM_PAIR
-#define MUON_GEMM_PAIR 1
-#endif
 // Paired-SM MMAs (tcgen05 cta_group::2): each CTA holds half of B, so a stage is 32 KB and five fit
 // beside the 64 KB of epilogue staging.
-constexpr bool kPairMma = MUON_GEMM_PAIR != 0;
-constexpr int kGramBN = 256, kGramStages = kPairMma ? 5 : 3;
-constexpr int kCombBN = 256, kCombStages = kPairMma ? 5 : 3;
-constexpr int kCluster = 2;  // the two CTAs that share one B block
+constexpr int kGramBN = 256, kGramStages = 5;
+constexpr int kCombBN = 256, kCombStages = 5;
 // Kernel parameters are limited to 32764 bytes.
 static_assert(sizeof(GemmArgs) + sizeof(FinalArgs<kMaxFinal>) <= 32764, "GEMM parameter block too large");
-using GramShape = GemmShape<true, kGramBN, kGramStages, kPairMma>;
-using CombShape = GemmShape<false, kCombBN, kCombStages, kPairMma>;
+using GramShape = GemmShape<true, kGramBN, kGramStages>;
+using CombShape = GemmShape<false, kCombBN, kCombStages>;
 
 constexpr int64_t kMaxDim = 1 << 20;          // rows or cols
 constexpr int64_t kMaxShort = 32768;          // min(rows, cols): the n x n Gram lives in workspace
@@ -168,6 +163,7 @@ struct Plan {
   std::vector<GemmBatch> batches;
   uint8_t* ws = nullptr;
   size_t ws_bytes = 0;
+  size_t dev_bytes = 0;  // device memory this plan holds (workspace and tile schedules)
   float* partial = nullptr;
   int* tickets = nullptr;
   float* inv = nullptr;
@@ -207,6 +203,9 @@ struct muon_ctx {
   };
   std::vector<Rec> recs;
   std::vector<cudaEvent_t> event_pool;
+  // Device memory held by the plans, and the cap on it (0: none; muon_set_workspace_limit).
+  size_t plan_bytes = 0;
+  size_t plan_limit = 0;
 };
 
 namespace {
@@ -377,7 +376,7 @@ void build_tiles(const std::vector<Group>& groups, int g0, int ng, int max_lists
   comb = lpt_schedule(std::move(ct), max_lists);
 }
 
-void free_plan(Plan* p) {
+void free_plan(muon_handle h, Plan* p) {
   if (!p) return;
   if (p->ws) cudaFree(p->ws);
   if (p->tiles_dev) cudaFree(p->tiles_dev);
@@ -385,6 +384,20 @@ void free_plan(Plan* p) {
   p->ws = nullptr;
   p->tiles_dev = nullptr;
   p->begin_dev = nullptr;
+  h->plan_bytes -= p->dev_bytes;
+  p->dev_bytes = 0;
+}
+
+// cudaMalloc for plan memory. Past the handle's cap it fails the way an exhausted device does
+// (cudaErrorMemoryAllocation), so both take the same out-of-memory path.
+cudaError_t plan_malloc(muon_handle h, Plan& P, void** ptr, size_t bytes) {
+  if (h->plan_limit != 0 && h->plan_bytes + bytes > h->plan_limit) return cudaErrorMemoryAllocation;
+  const cudaError_t e = cudaMalloc(ptr, bytes);
+  if (e == cudaSuccess) {
+    P.dev_bytes += bytes;
+    h->plan_bytes += bytes;
+  }
+  return e;
 }
 
 muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t>>& key, Plan** out) {
@@ -424,9 +437,10 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
   const size_t post_off = take(P.mats.size() * 4 + 4);
   P.ws_bytes = off;
 
-  cudaError_t e = cudaMalloc(&P.ws, P.ws_bytes);
+  cudaError_t e = plan_malloc(h, P, reinterpret_cast<void**>(&P.ws), P.ws_bytes);
   if (e != cudaSuccess) {
     cudaGetLastError();
+    free_plan(h, &P);
     return fail(h, MUON_ERR_NOMEM, "workspace of %zu bytes: %s", P.ws_bytes, cudaGetErrorString(e));
   }
   P.partial = reinterpret_cast<float*>(P.ws + part_off);
@@ -435,7 +449,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
   P.post = reinterpret_cast<float*>(P.ws + post_off);
   e = cudaMemset(P.ws, 0, P.ws_bytes);
   if (e != cudaSuccess) {
-    free_plan(&P);
+    free_plan(h, &P);
     return cuda_fail(h, e, "workspace clear");
   }
 
@@ -467,18 +481,20 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
     P.batches.push_back(B);
   }
   if (!all_tiles.empty()) {
-    e = cudaMalloc(&P.tiles_dev, all_tiles.size() * sizeof(int4));
-    cudaError_t e2 = cudaMalloc(&P.begin_dev, all_begin.size() * sizeof(int));
+    e = plan_malloc(h, P, reinterpret_cast<void**>(&P.tiles_dev), all_tiles.size() * sizeof(int4));
+    cudaError_t e2 = e != cudaSuccess ? e
+                                      : plan_malloc(h, P, reinterpret_cast<void**>(&P.begin_dev),
+                                                    all_begin.size() * sizeof(int));
     if (e != cudaSuccess || e2 != cudaSuccess) {
       cudaGetLastError();
-      free_plan(&P);
+      free_plan(h, &P);
       return fail(h, MUON_ERR_NOMEM, "tile schedule: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
     }
     e = cudaMemcpy(P.tiles_dev, all_tiles.data(), all_tiles.size() * sizeof(int4), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
       e = cudaMemcpy(P.begin_dev, all_begin.data(), all_begin.size() * sizeof(int), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
-      free_plan(&P);
+      free_plan(h, &P);
       return cuda_fail(h, e, "tile schedule upload");
     }
   }
@@ -552,7 +568,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
       B.gram_aa.grp[gi] = GemmGroup{abuf, nullptr, g.n * g.ld_p, static_cast<int>(g.n), static_cast<int>(g.n),
                                     static_cast<int>(g.ld_p), static_cast<int>(ceil_div(g.n, 64))};
       if (!ok) {
-        free_plan(&P);
+        free_plan(h, &P);
         return fail(h, MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed for group %lld x %lld", (long long)g.n,
                     (long long)g.m);
       }
@@ -561,7 +577,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
   // The clear above ran on the legacy stream; the caller's stream may not be ordered after it.
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
-    free_plan(&P);
+    free_plan(h, &P);
     return cuda_fail(h, e, "plan synchronize");
   }
   *out = plan.get();
@@ -581,7 +597,7 @@ muon_status get_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t
     for (auto i = h->plans.begin(); i != h->plans.end(); ++i)
       if (i->second->last_use < victim->second->last_use) victim = i;
     cudaDeviceSynchronize();
-    free_plan(victim->second.get());
+    free_plan(h, victim->second.get());
     h->plans.erase(victim);
   }
   muon_status s = build_plan(h, key, out);
@@ -800,7 +816,7 @@ cudaLaunchConfig_t gemm_config(int lists, cudaStream_t s, cudaLaunchAttribute* a
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(lists * kCluster), 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = GemmShape<kGram, kBN, kStages, kPairMma>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = GemmShape<kGram, kBN, kStages>::SMEM_BYTES;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCluster;
@@ -824,9 +840,9 @@ muon_status launch_gemm(muon_handle h, const GemmArgs& a, const FinalArgs<kFinal
   if (h->profiling) {
     GemmArgs ap = a;
     ap.clk = h->clk_dev;
-    e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kCluster, kFinal, kPairMma>, ap, f);
+    e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kFinal>, ap, f);
   } else {
-    e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kCluster, kFinal, kPairMma>, a, f);
+    e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kGram, kBN, kStages, kFinal>, a, f);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -1163,9 +1179,9 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
     return MUON_ERR_CUDA;
   }
   h->clk_dev = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(h->err_dev) + 64);
-  auto kgram = ns_gemm_kernel<true, kGramBN, kGramStages, kCluster, false, kPairMma>;
-  auto kcomb = ns_gemm_kernel<false, kCombBN, kCombStages, kCluster, false, kPairMma>;
-  auto kfinal = ns_gemm_kernel<false, kCombBN, kCombStages, kCluster, true, kPairMma>;
+  auto kgram = ns_gemm_kernel<true, kGramBN, kGramStages, false>;
+  auto kcomb = ns_gemm_kernel<false, kCombBN, kCombStages, false>;
+  auto kfinal = ns_gemm_kernel<false, kCombBN, kCombStages, true>;
   cudaError_t e1 = cudaFuncSetAttribute(kgram, cudaFuncAttributeMaxDynamicSharedMemorySize, GramShape::SMEM_BYTES);
   cudaError_t e2 = cudaFuncSetAttribute(kcomb, cudaFuncAttributeMaxDynamicSharedMemorySize, CombShape::SMEM_BYTES);
   cudaError_t e3 = cudaFuncSetAttribute(kfinal, cudaFuncAttributeMaxDynamicSharedMemorySize, CombShape::SMEM_BYTES);
@@ -1174,9 +1190,9 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
     cudaFree(h->err_dev);
     return MUON_ERR_CUDA;
   }
-  // Persistent grids: as many tile lists as clusters (or CTAs) that can be resident at once.
+  // Persistent grids: as many tile lists as clusters that can be resident at once.
   h->max_lists = h->num_sms / kCluster;
-  if (kCluster > 1) {
+  {
     cudaLaunchAttribute attr[2];
     int n1 = 0, n2 = 0, n3 = 0;
     cudaLaunchConfig_t c1 = gemm_config<true, kGramBN, kGramStages>(1, nullptr, attr);
@@ -1200,7 +1216,7 @@ muon_status muon_destroy(muon_handle h) {
   {
     DeviceGuard guard(h->device);
     cudaDeviceSynchronize();
-    for (auto& kv : h->plans) free_plan(kv.second.get());
+    for (auto& kv : h->plans) free_plan(h, kv.second.get());
     if (h->err_dev) cudaFree(h->err_dev);
     for (auto& r : h->recs) {
       cudaEventDestroy(r.a);
@@ -1283,6 +1299,18 @@ muon_status muon_selftest_wait(muon_handle h, int64_t limit_ns, void* stream) {
   DeviceGuard guard(h->device);
   wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(h->err_dev, static_cast<uint64_t>(limit_ns));
   return launch_checked(h, "wait self-test kernel");
+}
+
+muon_status muon_set_workspace_limit(muon_handle h, int64_t bytes) {
+  if (!h || bytes < 0) return MUON_ERR_INVALID;
+  h->plan_limit = static_cast<size_t>(bytes);
+  return MUON_OK;
+}
+
+muon_status muon_workspace_bytes(muon_handle h, int64_t* bytes) {
+  if (!h || !bytes) return MUON_ERR_INVALID;
+  *bytes = static_cast<int64_t>(h->plan_bytes);
+  return MUON_OK;
 }
 
 muon_status muon_profile_enable(muon_handle h, int enable) {

@@ -12,9 +12,11 @@
 // per-matrix inverse norms, in g_noalloc_scratch. The array is part of the
 // library's device image: every GPU that loads the library holds it
 // (kNoAllocScratchBytes) until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -39,7 +41,16 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+// The scratch address per device, with the context it was looked up in: a context created again
+// (after cudaDeviceReset, say) can load the module at another address, so a changed context
+// triggers a fresh lookup.
+struct ScratchSlot {
+  CUcontext ctx = nullptr;
+  void* addr = nullptr;
+};
+ScratchSlot g_scratch_slot[kMaxDevices];
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
 
 void put(char* msg, int len, const char* text) {
   if (msg && len > 0) {
@@ -48,17 +59,40 @@ void put(char* msg, int len, const char* text) {
   }
 }
 
-// Device address of g_noalloc_scratch on the current device, looked up once per device.
-// In host code the array's name is only a stand-in; kernels must get this address.
+// Device address of g_noalloc_scratch on the current device, looked up once per device and
+// context (the first call on a device does it). In host code the array's name is only a stand-in;
+// kernels must get this address.
 muon_status scratch_for_current_device(void** out, char* msg, int len) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
     cudaGetLastError();
     put(msg, len, "no current CUDA device");
     return MUON_ERR_CUDA;
   }
+  if (dev >= kMaxDevices) {
+    char buf[128];
+    snprintf(buf, sizeof(buf), "device %d is beyond the %d devices this entry point keeps scratch addresses for",
+             dev, kMaxDevices);
+    put(msg, len, buf);
+    return MUON_ERR_UNSUPPORTED;
+  }
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_addr[dev]) {
+  if (!g_ctx_get_current) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      cudaGetLastError();
+      put(msg, len, "cuCtxGetCurrent entry point not found");
+      return MUON_ERR_CUDA;
+    }
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+  }
+  // Null while this thread has no context yet; the lookup below creates the device's primary context.
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  ScratchSlot& slot = g_scratch_slot[dev];
+  if (!slot.addr || !ctx || slot.ctx != ctx) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || !p) {
@@ -66,9 +100,14 @@ muon_status scratch_for_current_device(void** out, char* msg, int len) {
       put(msg, len, "cudaGetSymbolAddress of the scratch array failed");
       return MUON_ERR_CUDA;
     }
-    g_scratch_addr[dev] = p;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) {
+      put(msg, len, "no current CUDA context");
+      return MUON_ERR_CUDA;
+    }
+    slot.addr = p;
+    slot.ctx = ctx;
   }
-  *out = g_scratch_addr[dev];
+  *out = slot.addr;
   return MUON_OK;
 }
 

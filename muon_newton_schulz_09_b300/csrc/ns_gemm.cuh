@@ -23,13 +23,12 @@
 //
 // Structure: a persistent grid of 2-CTA clusters (one CTA per SM) walks a
 // host-built tile list covering every matrix of every shape group in the
-// batch. By default the pair runs paired-SM MMAs (tcgen05 cta_group::2,
-// M = 256): each CTA owns 128 rows of a 256 x 256 output tile and loads its
-// own A rows and half of B; built with kPair = false, each CTA runs M = 128
-// MMAs and the two share B through TMA multicast. Warp 0 issues TMA loads into
-// a ring of shared-memory stages, one thread of warp 1 (of the even CTA when
-// paired) issues tcgen05.mma into a double-buffered fp32 accumulator in
-// tensor memory, and warps 2-9 drain the accumulator (tcgen05.ld), apply the
+// batch. The pair runs paired-SM MMAs (tcgen05 cta_group::2, M = 256): each
+// CTA owns 128 rows of a 256 x 256 output tile and loads its own A rows and
+// its own half of B; no load is shared between the two CTAs. Warp 0 issues TMA
+// loads into a ring of shared-memory stages, one thread of warp 1 of the even
+// CTA issues tcgen05.mma into a double-buffered fp32 accumulator in tensor
+// memory of both CTAs, and warps 2-9 drain the accumulator (tcgen05.ld), apply the
 // epilogue and store bf16 to global memory by TMA. A host-built schedule gives
 // each cluster its own list of tiles, balanced by contraction length. Every
 // wait is bounded (see mbar_wait_bounded).
@@ -115,13 +114,13 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <bool kGram, int kBN, int kStages, bool kPair = false>
+template <bool kGram, int kBN, int kStages>
 struct GemmShape {
   static constexpr int BM = 128;
   static constexpr int BK = 64;
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   // Paired-SM MMAs: each CTA holds only its half of B's columns.
-  static constexpr uint32_t B_BYTES = (kPair ? kBN / 2 : kBN) * BK * 2;
+  static constexpr uint32_t B_BYTES = (kBN / 2) * BK * 2;
   static constexpr uint32_t TMEM_COLS = 2 * kBN;
   static constexpr uint32_t STAGING_BYTES = 4 * 16384;  // two 128 x 64 bf16 boxes per column half
   static constexpr uint32_t BAR_BYTES = 8 * (2 * kStages + 5 + 4) + 16;  // + one barrier per staging box
@@ -130,30 +129,24 @@ struct GemmShape {
 };
 
 // The two CTAs of a cluster take tile rows I and I+1 of the same tile column,
-// so they need the same B block.
-//
-// kPair = false (1-SM MMAs, M = 128): each CTA loads its own A and one half of
-// B, and multicasts that half into both CTAs' shared memory. A stage is refilled
-// only when both CTAs' MMAs have released it, so every MMA commit of a stage
-// arrives on that stage's empty barrier in both CTAs.
-//
-// kPair = true (paired-SM MMAs, tcgen05 cta_group::2, M = 256): each CTA loads
-// its own A rows and its own half of B's columns into its own shared memory,
-// signalling the even (leader) CTA's full barrier; the leader's single MMA
-// thread issues M = 256 MMAs that read both CTAs' shared memory and write each
-// CTA's 128 accumulator rows into its own TMEM. Commits multicast to both CTAs;
-// the odd CTA's epilogue releases the accumulator on the leader's barrier.
-template <bool kGram, int kBN, int kStages, int kCluster, bool kFinal, bool kPair = false>
+// so they need the same B block. Paired-SM MMAs (tcgen05 cta_group::2,
+// M = 256): each CTA loads its own A rows and its own half of B's columns into
+// its own shared memory, signalling the even (leader) CTA's full barrier; the
+// leader's single MMA thread issues M = 256 MMAs that read both CTAs' shared
+// memory and write each CTA's 128 accumulator rows into its own TMEM. Commits
+// arrive on the barrier at the same offset in both CTAs; the odd CTA's
+// epilogue releases the accumulator on the leader's barrier.
+constexpr int kCluster = 2;
+
+template <bool kGram, int kBN, int kStages, bool kFinal>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     ns_gemm_kernel(const __grid_constant__ GemmArgs args, const __grid_constant__ FinalArgs<kFinal ? kMaxFinal : 1> fin) {
-  using S = GemmShape<kGram, kBN, kStages, kPair>;
+  using S = GemmShape<kGram, kBN, kStages>;
   constexpr int BM = S::BM, BK = S::BK;
   constexpr uint32_t A_BYTES = S::A_BYTES, B_BYTES = S::B_BYTES;
-  constexpr uint32_t kIdesc = instr_desc_bf16(kPair ? 2 * BM : BM, kBN, !kGram);
+  constexpr uint32_t kIdesc = instr_desc_bf16(2 * BM, kBN, !kGram);
   constexpr uint16_t kPairMask = 0x3;
-  static_assert(!kPair || kCluster == 2, "paired-SM MMAs need clusters of two");
   static_assert(kBN == 256, "tile width");
-  static_assert(kCluster == 1 || kCluster == 2, "cluster size");
   static_assert(!(kGram && kFinal), "only the combine writes to the caller's matrices");
   static_assert(S::TMEM_COLS == 512, "TMEM allocation must be a power of two");
 
@@ -171,8 +164,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rank = kCluster == 2 ? static_cast<int>(cluster_cta_rank()) : 0;
-  const int list = blockIdx.x / kCluster;  // this CTA's (or cluster's) tile list
+  const int rank = static_cast<int>(cluster_cta_rank());
+  const int list = blockIdx.x / kCluster;  // this cluster's tile list
   const int t_begin = args.cta_begin[list], t_end = args.cta_begin[list + 1];
   const uint32_t bar0 = smem_u32(bars);
   // full[s]: stage s loaded; empty[s]: stage s consumed by the MMAs (of both CTAs);
@@ -187,12 +180,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(full_bar(st), 1);
-      mbar_init(empty_bar(st), kPair ? 1 : kCluster);
+      mbar_init(empty_bar(st), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      // Paired: one arrival per epilogue warp of both CTAs, on the leader's barrier.
-      mbar_init(tempty_bar(a), kPair ? 2 * (kEpilogueThreads / 32) : kEpilogueThreads);
+      // One arrival per epilogue warp of both CTAs, on the leader's barrier.
+      mbar_init(tempty_bar(a), 2 * (kEpilogueThreads / 32));
     }
     mbar_init(drain_bar, 1);
     for (int i = 0; i < 4; ++i) mbar_init(addend_bar(i), 1);
@@ -209,17 +202,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
   if (warp == 1) {
-    if constexpr (kPair) {
-      tmem_alloc_pair(smem_u32(tmem_slot), S::TMEM_COLS);  // with warp 1 of the peer CTA
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
-      tmem_relinquish();
-    }
+    tmem_alloc_pair(smem_u32(tmem_slot), S::TMEM_COLS);  // with warp 1 of the peer CTA
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
-  if (kCluster > 1) cluster_sync_all();  // the peer's barriers exist before anything is sent to them
+  cluster_sync_all();  // the peer's barriers exist before anything is sent to them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Everything above overlaps the previous kernel's tail; its outputs are read only below.
@@ -247,45 +235,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
-          if constexpr (kPair) {
-            // Both CTAs' loads complete on the leader's full barrier, which expects them all.
-            const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * bytes);
-            armed |= 1u << stage;
-            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-            if (!a_in_b)
-              tma_load_3d_pair(smem_u32(sA + stage * A_BYTES), ma, leader_full, kb * BK, I * BM, td.y);
-            const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
-            if (kGram) {  // this CTA's 128 of the 256 B rows
-              tma_load_3d_pair(b_dst, mb, leader_full, kb * BK, td.w * kBN + rank * 128, td.y);
-            } else {      // this CTA's 128 of the 256 B columns, two boxes of 64
-#pragma unroll
-              for (int c = 0; c < 2; ++c)
-                tma_load_3d_pair(b_dst + c * 8192u, mb, leader_full, td.w * kBN + rank * 128 + c * 64, kb * BK, td.y);
-            }
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-            continue;
-          }
-          mbar_arrive_expect_tx(full_bar(stage), bytes);
+          // Both CTAs' loads complete on the leader's full barrier, which expects them all.
+          const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * bytes);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          if (!a_in_b) tma_load_3d(smem_u32(sA + stage * A_BYTES), ma, full_bar(stage), kb * BK, I * BM, td.y);
+          if (!a_in_b)
+            tma_load_3d_pair(smem_u32(sA + stage * A_BYTES), ma, leader_full, kb * BK, I * BM, td.y);
           const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
-          // B in boxes: Gram two boxes of 128 rows (K-major), combine four boxes of 64 columns (MN-major).
-          constexpr int kBoxes = kGram ? 2 : 4;
-          constexpr uint32_t kBoxBytes = B_BYTES / kBoxes;
+          if (kGram) {  // this CTA's 128 of the 256 B rows
+            tma_load_3d_pair(b_dst, mb, leader_full, kb * BK, td.w * kBN + rank * 128, td.y);
+          } else {      // this CTA's 128 of the 256 B columns, two boxes of 64
 #pragma unroll
-          for (int c = 0; c < kBoxes; ++c) {
-            if (kCluster == 2 && (c * 2 / kBoxes) != rank) continue;  // the peer sends this half
-            const int x = kGram ? kb * BK : td.w * kBN + c * 64;
-            const int y = kGram ? td.w * kBN + c * 128 : kb * BK;
-            if (kCluster == 2)
-              tma_load_3d_multicast(b_dst + c * kBoxBytes, mb, full_bar(stage), x, y, td.y, kPairMask);
-            else
-              tma_load_3d(b_dst + c * kBoxBytes, mb, full_bar(stage), x, y, td.y);
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d_pair(b_dst + c * 8192u, mb, leader_full, td.w * kBN + rank * 128 + c * 64, kb * BK, td.y);
           }
           if (++stage == kStages) {
             stage = 0;
@@ -294,7 +257,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (!ok) break;
       }
-      if (*abort_flag && (!kPair || rank == 0)) {
+      if (*abort_flag && rank == 0) {
         // Let loads already issued land before the CTA's shared memory is released.
         for (int st = 0; st < kStages; ++st)
           if (armed & (1u << st)) mbar_wait_drain(full_bar(st), (armed_parity >> st) & 1u);
@@ -302,7 +265,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && (!kPair || rank == 0)) {
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -324,9 +287,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
-          // Paired: each CTA's B half holds its own 128 rows, so an A inside B is the whole half.
-          const uint32_t a_addr =
-              a_in_b ? b_addr + (kPair ? 0u : static_cast<uint32_t>(I & 1) * A_BYTES) : smem_u32(sA + stage * A_BYTES);
+          // Each CTA's B half holds its own 128 rows, so an A inside B is the whole half.
+          const uint32_t a_addr = a_in_b ? b_addr : smem_u32(sA + stage * A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             // K-major: the next 16 k-values are 32 bytes further along each 128-byte row.
@@ -334,38 +296,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // MN-major: the next 16 k-values are 16 rows (2048 bytes) further down.
             const uint64_t b_desc = kGram ? smem_desc_sw128(b_addr + k * 32u, 16u, 1024u)
                                           : smem_desc_sw128(b_addr + k * 2048u, 8192u, 1024u);
-            if constexpr (kPair)
-              mma_bf16_ss_pair(d_tmem, a_desc, b_desc, kIdesc, (kb | k) != 0 ? 1u : 0u);
-            else
-              mma_bf16_ss(d_tmem, a_desc, b_desc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            mma_bf16_ss_pair(d_tmem, a_desc, b_desc, kIdesc, (kb | k) != 0 ? 1u : 0u);
           }
           issued = true;
-          if constexpr (kPair)
-            mma_commit_pair_multicast(empty_bar(stage), kPairMask);
-          else if (kCluster == 2)
-            mma_commit_multicast(empty_bar(stage), kPairMask);
-          else
-            mma_commit(empty_bar(stage));
+          mma_commit_pair_multicast(empty_bar(stage), kPairMask);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if constexpr (kPair)
-          mma_commit_pair_multicast(tfull_bar(acc), kPairMask);
-        else
-          mma_commit(tfull_bar(acc));
+        mma_commit_pair_multicast(tfull_bar(acc), kPairMask);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       if (*abort_flag && issued) {
-        if constexpr (kPair)
-          mma_commit_pair_multicast(drain_bar, 0x1);
-        else
-          mma_commit(drain_bar);
+        mma_commit_pair_multicast(drain_bar, 0x1);
         mbar_wait_drain(drain_bar, 0);
       }
     }
@@ -605,12 +553,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         tc_fence_before();
-        if constexpr (kPair) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));  // the leader's barrier
-        } else {
-          mbar_arrive(tempty_bar(acc));
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));  // the leader's barrier
         released = true;
         const int mi = fin.first[td.x] + td.y;
         const bool tr = fin.trans[mi] != 0;
@@ -732,12 +676,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (*abort_flag) break;
       if (!released) {
         tc_fence_before();
-        if constexpr (kPair) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));  // the leader's barrier
-        } else {
-          mbar_arrive(tempty_bar(acc));
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));  // the leader's barrier
       }
       if (++acc == 2) {
         acc = 0;
@@ -753,14 +693,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   __syncthreads();
   // No CTA leaves while its peer may still deliver loads or MMA-commit arrivals into it.
-  if (kCluster > 1) cluster_sync_all();
+  cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    if constexpr (kPair)
-      tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
-    else
-      tmem_dealloc(tmem_base, S::TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
   }
   if (args.clk && threadIdx.x == 0) {
     atomicAdd(args.clk, static_cast<unsigned long long>(clock64() - clk_start));

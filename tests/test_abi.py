@@ -133,3 +133,10 @@ def test_create_rejects_a_bad_config_before_touching_a_gpu():
         lib.muon_default_config(ctypes.byref(cfg))
         setattr(cfg, field, value)
         assert lib.muon_create(ctypes.byref(h), 0, ctypes.byref(cfg)) == MUON_ERR_INVALID, field
+
+
+def test_workspace_limit_calls_reject_a_null_handle():
+    lib = mu.load_library()
+    v = ctypes.c_int64(-1)
+    assert lib.muon_set_workspace_limit(None, 1 << 20) == MUON_ERR_INVALID
+    assert lib.muon_workspace_bytes(None, ctypes.byref(v)) == MUON_ERR_INVALID

@@ -92,3 +92,25 @@ def test_reference_arm_small_workload(monkeypatch):
     line = bench.run_reference(bench.argparse.Namespace(workload="tiny", steps=4, warmup=3))
     assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_config_matches_ours(monkeypatch):
+    """Both arms print the same config object for the same workload, so their lines compare."""
+    w = wl.small_workload("tiny2", [(32, 64), (64, 32)], kind="step", grad_std=1e-3, seed=4)
+    monkeypatch.setitem(wl.WORKLOADS, "tiny2", w)
+    monkeypatch.delenv("RANK", raising=False)
+    line = bench.run_reference(bench.argparse.Namespace(workload="tiny2", steps=2, warmup=3))
+    assert line["config"] == bench.config_of(w, 1, False)
+    assert set(line["config"]) >= {"workload", "parallelism", "l2", "precise_carry", "alg_flops_per_step"}
+
+
+def test_peak_choice_follows_the_region_length():
+    """A region under a second is a kernel timed in a short burst: the burst peak applies."""
+    assert not bench.uses_sustained_peak(0.022)
+    assert not bench.uses_sustained_peak(0.6)
+    assert bench.uses_sustained_peak(1.0) and bench.uses_sustained_peak(30.0)
+
+
+def test_resident_bytes_of_the_headline_step():
+    # bf16 grads (2) + fp32 momentum (4) + bf16 params (2) per element
+    assert bench.resident_bytes(wl.GPT2_124M) == 84934656 * 8

@@ -415,3 +415,73 @@ def test_many_iterations_reach_the_polar_factor(muon):
         u, _, vt = np.linalg.svd(y.astype(np.float64), full_matrices=False)
         assert rel_f(gk, want) < TOL
         assert rel_f(gk, u @ vt) < 2e-2
+
+
+def test_step_without_shape_scaled_lr():
+    """scale_lr_by_shape = 0: every matrix takes the plain lr, tall ones included (fused update for the
+    bf16 params, the update kernel for the fp32 ones)."""
+    from muon_newton_schulz_09_b300 import Muon
+    shapes = [(384, 128), (128, 384), (130, 70)]
+    lr = 0.02
+    for param_dtype in ("bf16", "f32"):
+        w, g, m, p = step_case(shapes, "bf16", param_dtype, seed=27)
+        P = [dev(x, param_dtype) for x in p]
+        with Muon(0, scale_lr_by_shape=False) as m0:
+            m0.step(P, [dev(x, "bf16") for x in g], [dev(x, "f32") for x in m], lr=lr, beta=0.95, nesterov=True)
+            torch.cuda.synchronize()
+            assert m0.get_error() == 0
+        for j, (r, c) in enumerate(shapes):
+            w_new, _, o = oracle.muon_step(p[j], g[j], m[j], lr, 0.95, True, 5, CUBIC, scale_lr_by_shape=False)
+            upd = lr * np.abs(o).max()
+            err = np.abs(host(P[j]) - w_new)
+            ulp = bf16_ulp(w_new) if param_dtype == "bf16" else np.abs(w_new) * 2.0 ** -22
+            assert np.all(err <= ulp + 0.05 * upd), (param_dtype, r, c, float(err.max()))
+            # the shape-scaled update would differ by (sqrt(3) - 1) lr O on the 384 x 128 matrix
+            if r > c:
+                w_scaled, _, _ = oracle.muon_step(p[j], g[j], m[j], lr, 0.95, True, 5, CUBIC)
+                assert rel_f(host(P[j]) - p[j], w_scaled - p[j]) > 0.3
+
+
+def test_workspace_limit_gives_nomem_without_side_effects():
+    """A plan that would exceed the handle's device-memory cap fails as an exhausted cudaMalloc does:
+    MUON_ERR_NOMEM before any launch, the caller's tensors untouched, plans already built kept, and
+    the next call with room builds the plan and computes the right step."""
+    from muon_newton_schulz_09_b300 import MUON_ERR_NOMEM, Muon, MuonError
+    small = [(128, 256)]
+    shapes = [(256, 640), (640, 256), (130, 70)]
+    lr = 0.02
+    w, g, m, p = step_case(shapes, "bf16", "bf16", seed=28)
+    P = [dev(x, "bf16") for x in p]
+    G = [dev(x, "bf16") for x in g]
+    M = [dev(x, "f32") for x in m]
+    with Muon(0) as mw:
+        # a first plan fits under the cap and stays usable
+        xs = [dev(np.ones(s, np.float32), "bf16") for s in small]
+        outs = [torch.empty(s, device="cuda") for s in small]
+        mw.orthogonalize(xs, outs, steps=1)
+        torch.cuda.synchronize()
+        held = mw.workspace_bytes()
+        assert held > 0
+        mw.set_workspace_limit(held + 4096)
+        p0 = [t.clone() for t in P]
+        m0 = [t.clone() for t in M]
+        with pytest.raises(MuonError) as e:
+            mw.step(P, G, M, lr=lr, beta=0.95, nesterov=True)
+        assert e.value.status == MUON_ERR_NOMEM
+        torch.cuda.synchronize()
+        assert mw.get_error() == 0 and mw.workspace_bytes() == held
+        for a, b in zip(P + M, p0 + m0):
+            assert torch.equal(a, b)
+        mw.orthogonalize(xs, outs, steps=1)  # the earlier plan still runs
+        torch.cuda.synchronize()
+        assert rel_f(host(outs[0]), oracle.orthogonalize(np.ones(small[0]), 1, CUBIC)) < TOL
+        mw.set_workspace_limit(0)
+        mw.step(P, G, M, lr=lr, beta=0.95, nesterov=True)
+        torch.cuda.synchronize()
+        assert mw.get_error() == 0 and mw.workspace_bytes() > held
+    for j, (r, c) in enumerate(shapes):
+        w_new, buf_new, o = oracle.muon_step(p[j], g[j], m[j], lr, 0.95, True, 5, CUBIC)
+        upd = lr * oracle.lr_scale(r, c) * np.abs(o).max()
+        err = np.abs(host(P[j]) - w_new)
+        assert np.all(err <= bf16_ulp(w_new) + 0.05 * upd), (r, c, float(err.max()))
+        assert rel_f(host(M[j]), buf_new) < 1e-6

@@ -241,6 +241,32 @@ def test_lr_scale_via_step():
     np.testing.assert_allclose(w_new, -0.5 * math.sqrt(3.0) * g / 3.0, atol=1e-15)
 
 
+def test_lr_scale_off_via_step():
+    """scale_lr_by_shape = False: the same 3x1 column takes the plain lr, with no sqrt(3) factor."""
+    g = np.array([[1.0], [2.0], [2.0]])
+    w = np.array([[0.5], [-1.0], [0.25]])
+    w_new, _, o = mo.muon_step(w, g, np.zeros((3, 1)), 0.5, 0.0, False, 4, CUBIC, 0.0, False)
+    np.testing.assert_allclose(o, g / 3.0, atol=1e-15)
+    np.testing.assert_allclose(w_new, w - 0.5 * g / 3.0, atol=1e-15)
+    # the wide orientation is unaffected by the switch either way (max(1, r/c) = 1)
+    wide = np.array([[3.0, 4.0]])
+    a, _, _ = mo.muon_step(np.zeros((1, 2)), wide, np.zeros((1, 2)), 0.1, 0.0, False, 2, CUBIC, 0.0, True)
+    b, _, _ = mo.muon_step(np.zeros((1, 2)), wide, np.zeros((1, 2)), 0.1, 0.0, False, 2, CUBIC, 0.0, False)
+    np.testing.assert_allclose(a, [[-0.06, -0.08]], atol=1e-15)
+    np.testing.assert_allclose(b, a, atol=0)
+
+
+def test_rel_frobenius_hand_values():
+    """||x - ref||_F / ||ref||_F on a 2x2 worked by hand: the difference has norm 1 and ref has norm
+    sqrt(1 + 4 + 9 + 25) = sqrt(39). A dropped square root would give 1/39, the wrong denominator
+    (||x||_F = sqrt(30)) 1/sqrt(30). A zero reference gives the absolute error."""
+    x = np.array([[1.0, 2.0], [3.0, 4.0]])
+    ref = np.array([[1.0, 2.0], [3.0, 5.0]])
+    assert oracle.rel_frobenius(x, ref) == pytest.approx(1.0 / math.sqrt(39.0), rel=1e-15)
+    assert oracle.rel_frobenius(ref, ref) == 0.0
+    assert oracle.rel_frobenius(np.array([[3.0, 4.0]]), np.zeros((1, 2))) == pytest.approx(5.0, rel=1e-15)
+
+
 def test_weight_decay_closed_form():
     """W' = W (1 - lr wd) - lr s O, element by element: a 1x2 row (no transpose, s = 1) whose
     orthogonalised update is g/|g| exactly (a single row is its own polar factor at any step count)."""
