@@ -606,6 +606,99 @@ def run_reference(args) -> dict:
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_sharded(args) -> dict:
+    """The step sharded over the ranks (--sharded): one in-place NCCL reduce-scatter of every
+    rank's gradients, muon_step on each rank's own matrices, one in-place all-gather of the bf16
+    parameters. One step advances the whole model once, whatever the number of ranks, so value =
+    steps / the slowest rank's time (strong scaling)."""
+    import torch
+    import torch.distributed as dist
+    from muon_newton_schulz_09_b300 import ShardedMuon
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if not dist.is_initialized():
+        if world > 1:
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        else:
+            dist.init_process_group("nccl", store=dist.HashStore(), rank=0, world_size=1,
+                                    device_id=torch.device("cuda", local_rank))
+    w = workload_of(args.workload)
+    if w.kind != "step":
+        raise SystemExit("--sharded runs muon_step workloads")
+    a, b, c = w.coeffs
+    sm = ShardedMuon(w.shapes, rank, world, local_rank, lr=w.lr, beta=w.beta, nesterov=w.nesterov,
+                     steps=w.steps, a=a, b=b, c=c, eps=w.eps, scale_lr_by_shape=True)
+    for j in range(w.count):  # every rank holds the same local gradients: the sum is world x them
+        sm.params[j].copy_(torch.from_numpy(wl.parameter(w, j)))
+        sm.grads[j].copy_(torch.from_numpy(wl.gradient(w, j)))
+    for k, j in enumerate(sm.own):
+        sm.momentum[k].copy_(torch.from_numpy(wl.momentum_buffer(w, j)))
+    grads0 = sm.flat_grads.clone()
+    lo, hi = rank * sm.layout.segment, (rank + 1) * sm.layout.segment
+    stream = torch.cuda.current_stream()
+
+    def step():
+        # The reduce-scatter leaves the summed gradients in this rank's own segment; with more than
+        # one rank that segment gets the local gradients back (a device copy standing in for the
+        # backward pass that writes fresh ones). With one rank the reduce-scatter changes nothing.
+        if world > 1:
+            sm.flat_grads[lo:hi].copy_(grads0[lo:hi], non_blocking=True)
+        sm.step()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    if sm.muon.get_error() != 0:
+        raise RuntimeError("device error flag raised during the timed region")
+    max_s = reduce_max(start.elapsed_time(end) / 1e3)
+    value = args.steps / max_s
+
+    # end to end: each step uploads this rank's gradients from pinned host memory and reads the
+    # replicated parameters back, around the same sharded step
+    h_grads = grads0.cpu().pin_memory()
+    h_params = torch.empty(sm.flat_params.shape, dtype=sm.flat_params.dtype).pin_memory()
+    n_e2e = max(3, min(args.steps, 50))
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        sm.flat_grads.copy_(h_grads, non_blocking=True)
+        sm.step()
+        h_params.copy_(sm.flat_params, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3)
+    cfg = config_of(w, world, False)
+    cfg["parallelism"] = (f"sharded x{world}: whole matrices per rank, one reduce-scatter of gradients and "
+                          f"one all-gather of parameters per step (NCCL)")
+    cfg["owned_matrices"] = len(sm.own)
+    cfg["load_balance"] = round(max(sm.layout.load) / (sum(sm.layout.load) / world), 4)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 / args.steps, 4), "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generators; random-init weights, no dataset)", "config": cfg,
+        "e2e": {"value": round(n_e2e / e2e_s, 3), "unit": UNIT,
+                "h2d_bytes_per_step": h_grads.numel() * h_grads.element_size(),
+                "d2h_bytes_per_step": h_params.numel() * h_params.element_size()},
+        "clocks": clk.summary(), "impl": "ours-sharded",
+    }
+    sm.close()
+    return line
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -616,9 +709,14 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--precise-carry", action="store_true", help="carry X between iterations as bf16 hi + lo")
+    ap.add_argument("--sharded", action="store_true",
+                    help="shard whole matrices over the ranks between a reduce-scatter and an all-gather")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
-    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_sharded(args) if args.sharded else run_ours(args)
     if line and dist_env()[0] == 0:
         print(json.dumps(line), flush=True)
     import torch.distributed as dist

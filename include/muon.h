@@ -171,6 +171,31 @@ muon_status muon_plan_stats(const int64_t* rows, const int64_t* cols, int count,
                             int* groups, int64_t* gram_tiles, int64_t* combine_tiles,
                             double* flops_per_iter);
 
+/* ---------------------------------------------------------------- sharding across ranks
+ * Host-only, no GPU. The speedrun reduce-scatters gradients instead of
+ * all-reducing them (energy-efficiency article on Modded-NanoGPT,
+ * technical-evolution section; "How to train a GPT model in 3 minutes",
+ * system optimisations, distributed communication) and merges the attention
+ * and MLP parameters into one reduce_scatter call ("Muon Custom Sizing", in
+ * the related-article list of the record analysis of
+ * 2026-05-27_MuddGatedAndDC). With whole matrices as the unit, each of
+ * `world` ranks owns a subset, gets its summed gradients from one in-place
+ * reduce-scatter, runs muon_step on them, and one in-place all-gather
+ * replicates the updated parameters.
+ *
+ * For `count` matrices rows[j] x cols[j]: owner[j] is the owning rank,
+ * chosen longest-processing-time first by the algorithmic flops of one
+ * Newton-Schulz iteration (n(n+1)m + 2n^2m, + n^2(n+1) when with_c), so the
+ * ranks' loads (load[r], may be NULL, `world` entries) are balanced.
+ * offset[j] is the element offset of matrix j (stored densely, ld = cols) in
+ * a flat buffer of world * segment elements laid out rank-major: rank r's
+ * matrices sit in index order inside [r*segment, (r+1)*segment), each
+ * starting on a multiple of `align` elements. *segment is the common segment
+ * length (a multiple of align, at least align). Deterministic: every rank
+ * computes the same layout. Bad arguments give MUON_ERR_INVALID. */
+muon_status muon_shard_layout(const int64_t* rows, const int64_t* cols, int count, int world, int with_c,
+                              int64_t align, int* owner, int64_t* offset, int64_t* segment, double* load);
+
 /* Device-memory cap for the handle's plans (workspaces and tile schedules),
  * in bytes; 0 removes the cap (the default). A call that needs a new plan
  * which would take the plans past the cap fails with MUON_ERR_NOMEM, exactly

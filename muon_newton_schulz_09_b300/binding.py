@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "muon_kernel_name": (c.c_char_p, [c.c_int]),
         "muon_selftest_wait": (c.c_int, [c.c_void_p, c.c_int64, c.c_void_p]),
         "muon_set_workspace_limit": (c.c_int, [c.c_void_p, c.c_int64]),
+        "muon_shard_layout": (c.c_int, [P(c.c_int64), P(c.c_int64), c.c_int, c.c_int, c.c_int, c.c_int64,
+                                        P(c.c_int), P(c.c_int64), P(c.c_int64), P(c.c_double)]),
         "muon_workspace_bytes": (c.c_int, [c.c_void_p, P(c.c_int64)]),
         "muon_normalize_noalloc": (c.c_int, [P(MuonMatrix), P(MuonMatrix), c.c_int, c.c_float, c.c_void_p,
                                              c.c_char_p, c.c_int]),

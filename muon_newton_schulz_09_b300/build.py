@@ -15,7 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmuon.so")
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(CSRC, "muon_api.cu"), os.path.join(CSRC, "muon_noalloc.cu")]
+SOURCES = [os.path.join(CSRC, "muon_api.cu"), os.path.join(CSRC, "muon_noalloc.cu"),
+           os.path.join(CSRC, "muon_shard.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "ns_gemm.cuh", "elementwise.cuh")] + [
     os.path.join(ROOT, "include", "muon.h")]
 
