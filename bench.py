@@ -130,7 +130,8 @@ def kernel_work(w: wl.Workload, carry: bool = False) -> dict:
     comb = sum(2 * n * n * m for n, m in map(oriented, w.shapes)) * k
     aa = sum(n * n * (n + 1) for n, m in map(oriented, w.shapes)) * k
     work = {"gram_xxt": ("flops", float(gram)), "combine_ax_bx": ("flops", float(comb)),
-            "gram_aa": ("flops", float(aa))}
+            "gram_aa": ("flops", float(aa)),
+            "newton_schulz": ("flops", float(gram + comb + (aa if w.coeffs[2] != 0 else 0)))}
     if w.kind == "step":
         work.update({"momentum_norm": ("bytes", float(elems * (gb + 4 + 4 + 2 + lo))),
                      "scale_orient": ("bytes", float(elems * (2 + 2))),
@@ -543,7 +544,7 @@ def run_ours(args) -> dict:
         if "frac_per_cycle" in k:
             roofline["frac_per_cycle"] = round(k["frac_per_cycle"], 4)
     gpu_launches = int(sum(n for ms, n in prof.values()))
-    gemm_ms = sum(prof[n][0] for n in ("gram_xxt", "gram_aa", "combine_ax_bx"))
+    gemm_ms = sum(prof[n][0] for n in ("gram_xxt", "gram_aa", "combine_ax_bx", "newton_schulz"))
     gemm_tflops = step_flops(w) * args.steps / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
 
     line = {

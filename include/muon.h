@@ -97,7 +97,13 @@ typedef struct {
  * few dominant directions this cuts the distance to the exact iteration by
  * one to two orders of magnitude. It costs a second pair of X buffers in
  * the workspace, 4 more bytes per element in each combine pass, and combines
- * that stage their two 64-column units one after the other. */
+ * that stage their two 64-column units one after the other.
+ * persistent (0 or 1): 1 runs every Newton-Schulz iteration of a call in one
+ * persistent launch (up to 16 iterations per launch), whose clusters take the
+ * Gram and combine tiles of all matrices from host-built work lists and wait
+ * on per-matrix stage counters in global memory. 0 runs one launch per Gram
+ * and per combine phase over the whole batch. Both compute the same thing
+ * with the same roundings. */
 typedef struct {
   int32_t steps;
   float a, b, c;
@@ -105,10 +111,11 @@ typedef struct {
   int32_t scale_lr_by_shape;
   float weight_decay;
   int32_t precise_carry;
+  int32_t persistent;
 } muon_config;
 
 /* Fills *cfg with the defaults: steps 5, (a,b,c) = (1.5, -0.5, 0), eps 1e-7,
- * scale_lr_by_shape 1, weight_decay 0, precise_carry 0. The cubic coefficients
+ * scale_lr_by_shape 1, weight_decay 0, precise_carry 0, persistent 1. The cubic coefficients
  * are the iteration's textbook form; the pages give none. */
 void muon_default_config(muon_config* cfg);
 
@@ -207,6 +214,22 @@ muon_status muon_shard_layout(const int64_t* rows, const int64_t* cols, int coun
 muon_status muon_set_workspace_limit(muon_handle h, int64_t bytes);
 muon_status muon_workspace_bytes(muon_handle h, int64_t* bytes);
 
+/* Host-only, no GPU: the work lists of the persistent Newton-Schulz launch
+ * (muon_config.persistent) for `count` matrices rows[j] x cols[j], `steps`
+ * iterations (1 .. 16, one launch) and `clusters` 2-CTA clusters, as the
+ * library builds them. An item is 4 int32: kind | group << 2 | flags << 12
+ * (kind 0 Gram X X^T, 1 Gram A A, 2 combine; flags 1 first iteration,
+ * 2 last iteration, 4 X in the second buffer), the matrix within its shape
+ * group (groups are the distinct oriented shapes, in order of first
+ * appearance), tile row | tile column << 16, and the number of finished
+ * epilogue halves (four per tile) of the matrix the item waits for. Cluster c
+ * takes items[begin[c] .. begin[c+1]) in order. Writes the item count to
+ * *num_items; with items and begin NULL nothing else is written, otherwise
+ * items needs room for 4 * *num_items values and begin for clusters + 1. */
+muon_status muon_persistent_schedule(const int64_t* rows, const int64_t* cols, int count, int steps, int with_c,
+                                     int clusters, int32_t* items, int64_t items_cap, int32_t* begin,
+                                     int64_t* num_items);
+
 /* Failure-detection self-test. Launches one kernel on `stream` that waits,
  * through the same bounded wait the GEMM kernels use, on a barrier that
  * nothing ever arrives at. After limit_ns (1e6 .. 2e9 ns, else
@@ -220,9 +243,10 @@ muon_status muon_selftest_wait(muon_handle h, int64_t limit_ns, void* stream);
  * muon_profile_read synchronises those events, writes per kernel kind the
  * summed milliseconds and launch counts since the last read (arrays of
  * MUON_KERNEL_KINDS entries, either may be NULL) and resets the sums. */
-#define MUON_KERNEL_KINDS 8
+#define MUON_KERNEL_KINDS 9
 /* kernel kinds: 0 momentum+norm, 1 norm, 2 scale+orient, 3 Gram X X^T,
- * 4 Gram A A (c != 0), 5 combine a X + B X, 6 update, 7 copy out */
+ * 4 Gram A A (c != 0), 5 combine a X + B X, 6 update, 7 copy out,
+ * 8 every Newton-Schulz iteration in one persistent launch */
 muon_status muon_profile_enable(muon_handle h, int enable);
 muon_status muon_profile_read(muon_handle h, double* ms, int64_t* launches);
 const char* muon_kernel_name(int kind);

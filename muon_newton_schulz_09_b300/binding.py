@@ -18,7 +18,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "muon.h")
 
 MUON_OK, MUON_ERR_INVALID, MUON_ERR_CUDA, MUON_ERR_NOMEM, MUON_ERR_UNSUPPORTED, MUON_ERR_TIMEOUT = range(6)
 MUON_F32, MUON_BF16 = 0, 1
-KERNEL_KINDS = 8
+KERNEL_KINDS = 9
 
 
 class MuonError(RuntimeError):
@@ -35,7 +35,7 @@ class MuonMatrix(ctypes.Structure):
 class MuonConfig(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_int32), ("a", ctypes.c_float), ("b", ctypes.c_float), ("c", ctypes.c_float),
                 ("eps", ctypes.c_float), ("scale_lr_by_shape", ctypes.c_int32), ("weight_decay", ctypes.c_float),
-                ("precise_carry", ctypes.c_int32)]
+                ("precise_carry", ctypes.c_int32), ("persistent", ctypes.c_int32)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "muon_kernel_name": (c.c_char_p, [c.c_int]),
         "muon_selftest_wait": (c.c_int, [c.c_void_p, c.c_int64, c.c_void_p]),
         "muon_set_workspace_limit": (c.c_int, [c.c_void_p, c.c_int64]),
+        "muon_persistent_schedule": (c.c_int, [P(c.c_int64), P(c.c_int64), c.c_int, c.c_int, c.c_int, c.c_int,
+                                               P(c.c_int32), c.c_int64, P(c.c_int32), P(c.c_int64)]),
         "muon_shard_layout": (c.c_int, [P(c.c_int64), P(c.c_int64), c.c_int, c.c_int, c.c_int, c.c_int64,
                                         P(c.c_int), P(c.c_int64), P(c.c_int64), P(c.c_double)]),
         "muon_workspace_bytes": (c.c_int, [c.c_void_p, P(c.c_int64)]),
@@ -165,6 +167,28 @@ def plan_stats(shapes: Sequence, with_c: bool = False) -> dict:
     return {"groups": g.value, "gram_tiles": gt.value, "combine_tiles": ct.value, "flops_per_iter": fl.value}
 
 
+def persistent_schedule(shapes: Sequence, steps: int, with_c: bool = False, clusters: int = 74):
+    """(items, begin) of the persistent launch's work lists (host only): items as an N x 4 list of
+    [kind | group << 2 | flags << 12, matrix in group, row | col << 16, counter target]."""
+    lib = load_library()
+    n = len(shapes)
+    rows = (ctypes.c_int64 * max(1, n))(*[int(r) for r, _ in shapes])
+    cols = (ctypes.c_int64 * max(1, n))(*[int(c) for _, c in shapes])
+    cnt = ctypes.c_int64()
+    st = lib.muon_persistent_schedule(rows, cols, n, int(steps), int(bool(with_c)), int(clusters), None, 0, None,
+                                      ctypes.byref(cnt))
+    if st != MUON_OK:
+        raise MuonError(st, "muon_persistent_schedule")
+    items = (ctypes.c_int32 * max(4, 4 * cnt.value))()
+    begin = (ctypes.c_int32 * (clusters + 1))()
+    st = lib.muon_persistent_schedule(rows, cols, n, int(steps), int(bool(with_c)), int(clusters), items,
+                                      cnt.value, begin, ctypes.byref(cnt))
+    if st != MUON_OK:
+        raise MuonError(st, "muon_persistent_schedule")
+    flat = list(items[:4 * cnt.value])
+    return [flat[4 * i:4 * i + 4] for i in range(cnt.value)], list(begin)
+
+
 def _stream_ptr(stream, device) -> ctypes.c_void_p:
     import torch
     if stream is None:
@@ -196,11 +220,11 @@ class Muon:
 
     def __init__(self, device: int = 0, steps: int = 5, a: float = 1.5, b: float = -0.5, c: float = 0.0,
                  eps: float = 1e-7, scale_lr_by_shape: bool = True, weight_decay: float = 0.0,
-                 precise_carry: bool = False):
+                 precise_carry: bool = False, persistent: bool = True):
         self.lib = load_library()
         self.device = device
         self.config = MuonConfig(steps, a, b, c, eps, int(bool(scale_lr_by_shape)), weight_decay,
-                                 int(bool(precise_carry)))
+                                 int(bool(precise_carry)), int(bool(persistent)))
         h = ctypes.c_void_p()
         st = self.lib.muon_create(ctypes.byref(h), device, ctypes.byref(self.config))
         if st != MUON_OK:

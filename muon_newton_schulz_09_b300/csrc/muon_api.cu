@@ -26,6 +26,7 @@
 
 #include "../../include/muon.h"
 #include "elementwise.cuh"
+#include "ns_fused.cuh"
 #include "ns_gemm.cuh"
 
 using namespace muon;
@@ -40,17 +41,34 @@ constexpr int kCombBN = 256, kCombStages = 5;
 static_assert(sizeof(GemmArgs) + sizeof(FinalArgs<kMaxFinal>) <= 32764, "GEMM parameter block too large");
 using GramShape = GemmShape<true, kGramBN, kGramStages>;
 using CombShape = GemmShape<false, kCombBN, kCombStages>;
+// The persistent launch running every iteration (ns_fused.cuh).
+constexpr int kFusedStages = 5;
+using FusedShape = GemmShape<true, 256, kFusedStages>;
+static_assert(sizeof(FusedArgs) + sizeof(FinalArgs<kMaxFinal>) <= 32764, "fused parameter block too large");
+// The persistent schedule's model, in units of one 64-wide k-block of a 256 x 256 tile (512
+// tensor-core cycles of the pair):
+// matrix state (both X buffers, B, A) admitted at once. Larger budgets schedule better: with
+// 150 MB the GPT-2 124M step took 1.0906 ms, with 512 MB 1.0867 ms and with 2 GB 1.0708 ms, so the
+// cap matters only for batches far larger than that set;
+constexpr double kFusedL2Budget = 512e6;
+// what a tile occupies its cluster for beyond its MMAs;
+constexpr int kFusedTileOverhead = 3;
+// from a tile's last MMA until the next stage of its matrix can use the result (epilogue drain,
+// store, counter, first operand loads). Planned with 32, the lists left the producers waiting on
+// counters about 7% of the kernel on the GPT-2 124M step; with 0, 44%.
+constexpr double kFusedLatency = 32.0;
 
 constexpr int64_t kMaxDim = 1 << 20;          // rows or cols
 constexpr int64_t kMaxShort = 32768;          // min(rows, cols): the n x n Gram lives in workspace
 constexpr int64_t kMaxElems = 1ll << 32;      // rows * cols
 constexpr int kMaxSteps = 100000;
 
-const char* kKernelNames[MUON_KERNEL_KINDS] = {"momentum_norm", "norm",          "scale_orient", "gram_xxt",
-                                               "gram_aa",       "combine_ax_bx", "update",       "copy_out"};
+const char* kKernelNames[MUON_KERNEL_KINDS] = {"momentum_norm", "norm",   "scale_orient", "gram_xxt",
+                                               "gram_aa",       "combine_ax_bx", "update", "copy_out",
+                                               "newton_schulz"};
 
 enum Kind { K_MOMENTUM = 0, K_NORM = 1, K_SCALE = 2, K_GRAM = 3, K_GRAM_AA = 4, K_COMBINE = 5, K_UPDATE = 6,
-            K_COPY = 7 };
+            K_COPY = 7, K_FUSED = 8 };
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
@@ -180,6 +198,21 @@ struct Plan {
   };
   std::vector<UserMap> user_maps;
   std::vector<std::unique_ptr<FinalArgs<kMaxFinal>>> fin;
+  // The persistent launch: tensor maps [group][role] and group table in device memory, per-matrix
+  // stage counters and the finish ticket in the workspace, and one item schedule per
+  // (iteration count, c != 0), built on first use.
+  CUtensorMap* maps_dev = nullptr;
+  NsGroup* groups_dev = nullptr;
+  int* counters = nullptr;
+  unsigned int* done = nullptr;
+  struct FusedSchedule {
+    int4* items = nullptr;
+    int* begin = nullptr;
+    int grid = 0;      // clusters
+    size_t bytes = 0;
+  };
+  std::map<std::pair<int, int>, FusedSchedule> fused;
+  std::unique_ptr<FinalArgs<kMaxFinal>> fin_slots;  // the last combine's caller maps, by matrix slot
 };
 
 }  // namespace
@@ -206,6 +239,7 @@ struct muon_ctx {
   // Device memory held by the plans, and the cap on it (0: none; muon_set_workspace_limit).
   size_t plan_bytes = 0;
   size_t plan_limit = 0;
+  bool per_phase = false;  // one launch per Gram / combine phase instead of the persistent launch
 };
 
 namespace {
@@ -381,9 +415,15 @@ void free_plan(muon_handle h, Plan* p) {
   if (p->ws) cudaFree(p->ws);
   if (p->tiles_dev) cudaFree(p->tiles_dev);
   if (p->begin_dev) cudaFree(p->begin_dev);
+  if (p->maps_dev) cudaFree(p->maps_dev);
+  for (auto& kv : p->fused)  // items and list offsets share one allocation
+    if (kv.second.items) cudaFree(kv.second.items);
+  p->fused.clear();
   p->ws = nullptr;
   p->tiles_dev = nullptr;
   p->begin_dev = nullptr;
+  p->maps_dev = nullptr;
+  p->groups_dev = nullptr;
   h->plan_bytes -= p->dev_bytes;
   p->dev_bytes = 0;
 }
@@ -435,6 +475,8 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
   const size_t tick_off = take(P.mats.size() * 4 + 4);
   const size_t inv_off = take(P.mats.size() * 4 + 4);
   const size_t post_off = take(P.mats.size() * 4 + 4);
+  const size_t cnt_off = take(P.mats.size() * 4 + 4);
+  const size_t done_off = take(16);
   P.ws_bytes = off;
 
   cudaError_t e = plan_malloc(h, P, reinterpret_cast<void**>(&P.ws), P.ws_bytes);
@@ -447,6 +489,8 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
   P.tickets = reinterpret_cast<int*>(P.ws + tick_off);
   P.inv = reinterpret_cast<float*>(P.ws + inv_off);
   P.post = reinterpret_cast<float*>(P.ws + post_off);
+  P.counters = reinterpret_cast<int*>(P.ws + cnt_off);
+  P.done = reinterpret_cast<unsigned int*>(P.ws + done_off);
   e = cudaMemset(P.ws, 0, P.ws_bytes);
   if (e != cudaSuccess) {
     free_plan(h, &P);
@@ -574,6 +618,52 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
       }
     }
   }
+  // Tensor maps and group table of the persistent launch.
+  if (!P.groups.empty()) {
+    const size_t ng = P.groups.size();
+    std::vector<CUtensorMap> maps(ng * kNumRoles);
+    std::vector<NsGroup> gt(ng);
+    for (size_t gi = 0; gi < ng; ++gi) {
+      const Group& g = P.groups[gi];
+      CUtensorMap* m = &maps[gi * kNumRoles];
+      uint8_t* xb[2] = {P.ws + g.x_off[0], P.ws + g.x_off[1]};
+      uint8_t* pbuf = P.ws + g.p_off;
+      uint8_t* abuf = P.ws + g.a_off;
+      bool ok = true;
+      for (int t = 0; t < 2; ++t) {
+        ok &= encode_map(h, &m[kRoleX0 + t], xb[t], g.m, g.n, g.count, g.ld_x, 64, 128);
+        ok &= encode_map(h, &m[kRoleXmn0 + t], xb[t], g.m, g.n, g.count, g.ld_x, 64, 64);
+        // Without the precise carry the low-part roles are never used; they hold valid maps of X.
+        uint8_t* lb = h->cfg.precise_carry ? P.ws + g.lo_off[t] : xb[t];
+        ok &= encode_map(h, &m[kRoleLo0 + t], lb, g.m, g.n, g.count, g.ld_x, 64, 128);
+      }
+      ok &= encode_map(h, &m[kRoleP], pbuf, g.n, g.n, g.count, g.ld_p, 64, 128);
+      ok &= encode_map(h, &m[kRolePm], pbuf, g.n, g.n, g.count, g.ld_p, 128, 64, false);
+      ok &= encode_map(h, &m[kRoleA], abuf, g.n, g.n, g.count, g.ld_p, 64, 128);
+      ok &= encode_map(h, &m[kRoleAm], abuf, g.n, g.n, g.count, g.ld_p, 128, 64, false);
+      if (!ok) {
+        free_plan(h, &P);
+        return fail(h, MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed for group %lld x %lld", (long long)g.n,
+                    (long long)g.m);
+      }
+      gt[gi] = NsGroup{static_cast<int>(g.n), static_cast<int>(g.m), g.count, g.first_slot,
+                       static_cast<int>(ceil_div(g.m, 64)), static_cast<int>(ceil_div(g.n, 64))};
+    }
+    const size_t mb = maps.size() * sizeof(CUtensorMap), gb = gt.size() * sizeof(NsGroup);
+    e = plan_malloc(h, P, reinterpret_cast<void**>(&P.maps_dev), mb + gb);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      free_plan(h, &P);
+      return fail(h, MUON_ERR_NOMEM, "tensor maps: %s", cudaGetErrorString(e));
+    }
+    P.groups_dev = reinterpret_cast<NsGroup*>(reinterpret_cast<uint8_t*>(P.maps_dev) + mb);
+    e = cudaMemcpy(P.maps_dev, maps.data(), mb, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(P.groups_dev, gt.data(), gb, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      free_plan(h, &P);
+      return cuda_fail(h, e, "tensor map upload");
+    }
+  }
   // The clear above ran on the legacy stream; the caller's stream may not be ordered after it.
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -641,9 +731,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-muon_status launch_checked(muon_handle h, const char* what) {
+// The result of one launch: its own return code (an error left over from an unrelated earlier
+// call is not this launch's failure), then the launch error state, which it clears.
+muon_status launch_checked(muon_handle h, cudaError_t launch, const char* what) {
   const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(h, e, what);
+  if (launch != cudaSuccess) return cuda_fail(h, launch, what);
+  (void)e;
   return MUON_OK;
 }
 
@@ -668,13 +761,11 @@ muon_status launch_momentum(muon_handle h, const Plan& P, const muon_matrix* src
   auto flush = [&]() -> muon_status {
     if (a.count == 0) return MUON_OK;
     ProfScope ps(h, kStep ? K_MOMENTUM : K_NORM, s);
-    if (f32)
-      launch_pdl(momentum_norm_kernel<kStep, true>, blocks, kEwThreads, 0, s, a);
-    else
-      launch_pdl(momentum_norm_kernel<kStep, false>, blocks, kEwThreads, 0, s, a);
+    const cudaError_t e = f32 ? launch_pdl(momentum_norm_kernel<kStep, true>, blocks, kEwThreads, 0, s, a)
+                              : launch_pdl(momentum_norm_kernel<kStep, false>, blocks, kEwThreads, 0, s, a);
     a.count = 0;
     blocks = 0;
-    return launch_checked(h, "momentum/norm kernel");
+    return launch_checked(h, e, "momentum/norm kernel");
   };
   for (size_t j = 0; j < P.mats.size(); ++j) {
     const MatInfo& mi = P.mats[j];
@@ -724,18 +815,15 @@ muon_status launch_map_dispatch(muon_handle h, const MapArgs& a, int blocks, boo
                                 cudaStream_t s, int kind) {
   ProfScope ps(h, kind, s);
   // Only the scale pass reads the caller's (possibly fp32) matrices; the others read the bf16 workspace.
+  cudaError_t e;
   if constexpr (kMode == kScale) {
-    if (src_f32)
-      launch_pdl(map_kernel<kMode, true, false>, blocks, kEwThreads, 0, s, a);
-    else
-      launch_pdl(map_kernel<kMode, false, false>, blocks, kEwThreads, 0, s, a);
+    e = src_f32 ? launch_pdl(map_kernel<kMode, true, false>, blocks, kEwThreads, 0, s, a)
+                : launch_pdl(map_kernel<kMode, false, false>, blocks, kEwThreads, 0, s, a);
   } else {
-    if (dst_f32)
-      launch_pdl(map_kernel<kMode, false, true>, blocks, kEwThreads, 0, s, a);
-    else
-      launch_pdl(map_kernel<kMode, false, false>, blocks, kEwThreads, 0, s, a);
+    e = dst_f32 ? launch_pdl(map_kernel<kMode, false, true>, blocks, kEwThreads, 0, s, a)
+                : launch_pdl(map_kernel<kMode, false, false>, blocks, kEwThreads, 0, s, a);
   }
-  return launch_checked(h, "map kernel");
+  return launch_checked(h, e, "map kernel");
 }
 
 // kMode = kScale: src = the caller's input (orthogonalize), dst = X0 slot, oriented.
@@ -848,7 +936,7 @@ muon_status launch_gemm(muon_handle h, const GemmArgs& a, const FinalArgs<kFinal
     cudaGetLastError();
     return cuda_fail(h, e, "tcgen05 GEMM launch");
   }
-  return launch_checked(h, "tcgen05 GEMM kernel");
+  return launch_checked(h, cudaSuccess, "tcgen05 GEMM kernel");
 }
 
 const FinalArgs<1> kNoFinal = {};
@@ -958,6 +1046,279 @@ muon_status run_iterations(muon_handle h, const Plan& P, int steps, float a, flo
   return MUON_OK;
 }
 
+// ------------------------------------------------------------------ persistent launch
+
+// Iterations one persistent launch covers at most; longer runs take several launches. Even, so every
+// launch starts with X in buffer 0 or an even iteration's buffer, as its items assume.
+constexpr int kFusedMaxIters = 16;
+
+struct SimMatrix {
+  int slot = 0;
+  double bytes = 0.0, work = 0.0;
+  std::vector<std::vector<std::pair<int4, int>>> stages;  // per stage: (item, modelled cost)
+  std::vector<double> path;  // per stage: the longest chain from its start to the matrix's end
+};
+
+// The items of `iters` iterations of every matrix, in the order a list-scheduling simulation of
+// `clusters` clusters takes them. A matrix's stages are, per iteration: the Gram tiles (upper
+// triangle, 256 x 256 pairs), the A A tiles when c != 0, the combine tiles. A stage may start once
+// its matrix's previous stage has ended (the item's counter target is the number of epilogue halves
+// of the earlier stages). Matrices enter in decreasing order of work, and a new one enters only
+// while the state of those in flight (both X buffers, B, A) fits kFusedL2Budget, or when nothing
+// else can run. A free cluster takes the item that can start soonest (the earliest admitted
+// matrix on ties). Each cluster's list keeps the simulation's order, which every dependency
+// respects: an item's stage begins only after all items of the stage before it were placed.
+void fused_schedule(const Plan& P, bool carry, int iters, bool c_nz, int clusters, std::vector<int4>& items,
+                    std::vector<int>& begin) {
+  std::vector<SimMatrix> mats;
+  for (size_t gi = 0; gi < P.groups.size(); ++gi) {
+    const Group& g = P.groups[gi];
+    const int nt = static_cast<int>(ceil_div(g.n, 128)), gt2 = static_cast<int>(ceil_div(g.n, 256));
+    const int mt = static_cast<int>(ceil_div(g.m, 256));
+    const int nk_m = static_cast<int>(ceil_div(g.m, 64)), nk_n = static_cast<int>(ceil_div(g.n, 64));
+    for (int b = 0; b < g.count; ++b) {
+      SimMatrix M;
+      M.slot = g.first_slot + b;
+      M.bytes = 2.0 * static_cast<double>(g.n * g.ld_x) * 2.0 * (carry ? 2.0 : 1.0) +
+                static_cast<double>(g.n * g.ld_p) * 2.0 * (c_nz ? 2.0 : 1.0);
+      int halves = 0;  // epilogue halves of the stages placed so far
+      for (int it = 0; it < iters; ++it) {
+        const int flags = (it == 0 ? kNsFirst : 0) | (it == iters - 1 ? kNsLast : 0) | ((it & 1) ? kNsOdd : 0);
+        auto gram_stage = [&](int kind, int nk) {
+          std::vector<std::pair<int4, int>> st;
+          for (int J = 0; J < gt2; ++J)
+            for (int I = 0; I < std::min(2 * J + 2, nt); I += kCluster)
+              st.push_back({ns_item(kind, static_cast<int>(gi), flags, b, I, J, halves), nk + kFusedTileOverhead});
+          halves += 4 * static_cast<int>(st.size());
+          M.stages.push_back(std::move(st));
+        };
+        gram_stage(kNsGram, nk_m);
+        if (c_nz) gram_stage(kNsGramAA, nk_n);
+        std::vector<std::pair<int4, int>> st;
+        for (int I = 0; I < nt; I += kCluster)
+          for (int J = 0; J < mt; ++J)
+            st.push_back({ns_item(kNsComb, static_cast<int>(gi), flags, b, I, J, halves), nk_n + kFusedTileOverhead});
+        halves += 4 * static_cast<int>(st.size());
+        M.stages.push_back(std::move(st));
+      }
+      for (const auto& st : M.stages)
+        for (const auto& x : st) M.work += x.second;
+      M.path.assign(M.stages.size() + 1, 0.0);
+      for (size_t q = M.stages.size(); q-- > 0;) {
+        int longest = 0;
+        for (const auto& x : M.stages[q]) longest = std::max(longest, x.second);
+        M.path[q] = M.path[q + 1] + longest + kFusedLatency;
+      }
+      mats.push_back(std::move(M));
+    }
+  }
+  std::vector<int> order(mats.size());
+  for (size_t j = 0; j < mats.size(); ++j) order[j] = static_cast<int>(j);
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return mats[x].work > mats[y].work; });
+
+  const int C = std::max(1, clusters);
+  using Ev = std::pair<double, int>;
+  std::priority_queue<Ev, std::vector<Ev>, std::greater<Ev>> freeq;
+  for (int c = 0; c < C; ++c) freeq.push({0.0, c});
+  std::vector<std::vector<int4>> per(static_cast<size_t>(C));
+  struct State {
+    size_t stage = 0, next = 0;
+    double ready = 0.0, end = 0.0;
+    bool finished = false;
+  };
+  std::vector<State> st(mats.size());
+  std::vector<int> active;
+  size_t admitted = 0, finished = 0;
+  double act_bytes = 0.0;
+  while (finished < mats.size()) {
+    const Ev top = freeq.top();
+    freeq.pop();
+    const double t = top.first;
+    // Among the items that can start now, the one with the longest chain still ahead of its matrix;
+    // if none can, the same among those that must wait.
+    int best = -1;
+    double best_start = 0.0;
+    bool best_now = false;
+    for (int j : active) {
+      if (st[j].finished) continue;
+      const double start = std::max(t, st[j].ready);
+      const bool now = start <= t;
+      if (best < 0 || (now && !best_now) ||
+          (now == best_now && mats[j].path[st[j].stage] > mats[best].path[st[best].stage])) {
+        best = j;
+        best_start = start;
+        best_now = now;
+      }
+    }
+    if ((best < 0 || best_start > t) && admitted < order.size() &&
+        (best < 0 || act_bytes + mats[order[admitted]].bytes <= kFusedL2Budget)) {
+      const int j = order[admitted++];
+      active.push_back(j);
+      act_bytes += mats[j].bytes;
+      freeq.push(top);
+      continue;
+    }
+    SimMatrix& M = mats[best];
+    State& s = st[best];
+    const auto& stage = M.stages[s.stage];
+    const auto& x = stage[s.next++];
+    const double end = best_start + x.second;
+    per[top.second].push_back(x.first);
+    // The cluster is free at `end`, but the item's result lands (and its matrix's next stage may
+    // start) only once the epilogue has drained it and the next item's operands have arrived.
+    s.end = std::max(s.end, end + kFusedLatency);
+    if (s.next == stage.size()) {
+      s.ready = s.end;
+      ++s.stage;
+      s.next = 0;
+      if (s.stage == M.stages.size()) {
+        s.finished = true;
+        ++finished;
+        act_bytes -= M.bytes;
+      }
+    }
+    freeq.push({end, top.second});
+  }
+  items.clear();
+  begin.assign(1, 0);
+  for (const auto& l : per) {
+    items.insert(items.end(), l.begin(), l.end());
+    begin.push_back(static_cast<int>(items.size()));
+  }
+}
+
+// Fills the caller-matrix maps of the last combine by matrix slot (group order). False when a
+// matrix is not bf16, 16-byte aligned with ld a multiple of 8, or the batch has more than
+// kMaxFinal matrices: the separate update / copy kernel then writes the caller's matrices.
+bool prepare_final_slots(muon_handle h, Plan& P, const muon_matrix* user, bool update, float lr) {
+  int slots = 0;
+  for (const Group& g : P.groups) slots += g.count;
+  if (slots > kMaxFinal) return false;
+  for (size_t j = 0; j < P.mats.size(); ++j) {
+    if (P.mats[j].skip) continue;
+    const muon_matrix& u = user[j];
+    if (u.dtype != MUON_BF16 || !aligned16(u.ptr) || u.ld % 8 != 0) return false;
+  }
+  if (!P.fin_slots) P.fin_slots = std::make_unique<FinalArgs<kMaxFinal>>();
+  if (P.user_maps.size() != P.mats.size()) P.user_maps.assign(P.mats.size(), Plan::UserMap{});
+  FinalArgs<kMaxFinal>& F = *P.fin_slots;
+  F.update = update ? 1 : 0;
+  F.keep = update ? 1.0f - lr * h->cfg.weight_decay : 1.0f;
+  for (size_t j = 0; j < P.mats.size(); ++j) {
+    const MatInfo& mi = P.mats[j];
+    if (mi.skip) continue;
+    const muon_matrix& u = user[j];
+    Plan::UserMap& um = P.user_maps[j];
+    if (um.ptr != u.ptr || um.ld != u.ld) {
+      const bool ok = mi.transposed
+                          ? encode_map(h, &um.map, u.ptr, mi.cols, mi.rows, 1, u.ld, 128, 64, false)
+                          : encode_map(h, &um.map, u.ptr, mi.cols, mi.rows, 1, u.ld, 64, 128, true);
+      if (!ok) {
+        um.ptr = nullptr;
+        return false;
+      }
+      um.ptr = u.ptr;
+      um.ld = u.ld;
+    }
+    F.map[mi.gslot] = um.map;
+    F.trans[mi.gslot] = mi.transposed ? 1 : 0;
+    const double sc = h->cfg.scale_lr_by_shape ? std::sqrt(std::max(1.0, double(mi.rows) / double(mi.cols))) : 1.0;
+    F.scale[mi.gslot] = update ? static_cast<float>(double(lr) * sc) : 0.f;
+  }
+  return true;
+}
+
+cudaLaunchConfig_t fused_config(int clusters, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCluster), 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = FusedShape::SMEM_BYTES;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
+// k Newton-Schulz iterations on X0 (buffer 0) in persistent launches of up to kFusedMaxIters
+// iterations each. Returns the buffer holding X_k. With `final_into_user` the last combine writes
+// the caller's matrices (prepare_final_slots); with `folded_scale` the first iteration applies the
+// per-matrix scale P.post.
+muon_status run_iterations_fused(muon_handle h, Plan& P, int steps, float a, float b, float c, cudaStream_t s,
+                                 int* xk, bool final_into_user, bool folded_scale) {
+  const bool c_nz = c != 0.0f;
+  int slots = 0;
+  for (const Group& g : P.groups) slots += g.count;
+  for (int i0 = 0; i0 < steps; i0 += kFusedMaxIters) {
+    const int iters = std::min(kFusedMaxIters, steps - i0);
+    const auto key = std::make_pair(iters, c_nz ? 1 : 0);
+    auto it = P.fused.find(key);
+    if (it == P.fused.end()) {
+      std::vector<int4> items;
+      std::vector<int> begin;
+      fused_schedule(P, h->cfg.precise_carry != 0, iters, c_nz, h->max_lists, items, begin);
+      Plan::FusedSchedule fs;
+      fs.grid = static_cast<int>(begin.size()) - 1;
+      const size_t ib = items.size() * sizeof(int4), bb = begin.size() * sizeof(int);
+      void* buf = nullptr;
+      cudaError_t e = plan_malloc(h, P, &buf, ib + bb);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, MUON_ERR_NOMEM, "persistent schedule of %zu bytes: %s", ib + bb, cudaGetErrorString(e));
+      }
+      fs.items = static_cast<int4*>(buf);
+      fs.begin = reinterpret_cast<int*>(static_cast<uint8_t*>(buf) + ib);
+      fs.bytes = ib + bb;
+      e = cudaMemcpy(fs.items, items.data(), ib, cudaMemcpyHostToDevice);
+      if (e == cudaSuccess) e = cudaMemcpy(fs.begin, begin.data(), bb, cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) {
+        cudaFree(buf);
+        P.dev_bytes -= ib + bb;
+        h->plan_bytes -= ib + bb;
+        return cuda_fail(h, e, "persistent schedule upload");
+      }
+      it = P.fused.emplace(key, fs).first;
+    }
+    const Plan::FusedSchedule& fs = it->second;
+    FusedArgs fa;
+    memset(&fa, 0, sizeof(fa));
+    fa.maps = P.maps_dev;
+    fa.groups = P.groups_dev;
+    fa.items = fs.items;
+    fa.begin = fs.begin;
+    fa.counters = P.counters;
+    fa.done = P.done;
+    fa.post = (folded_scale && i0 == 0) ? P.post : nullptr;
+    fa.num_slots = slots;
+    fa.num_groups = static_cast<int>(P.groups.size());
+    fa.c_nonzero = c_nz ? 1 : 0;
+    fa.a = a;
+    fa.b = b;
+    fa.c = c;
+    fa.carry = h->cfg.precise_carry ? 1 : 0;
+    fa.final_mode = (final_into_user && i0 + iters == steps) ? 1 : 0;
+    fa.err = h->err_dev;
+    fa.clk = h->profiling ? h->clk_dev : nullptr;
+    static const FinalArgs<kMaxFinal> kNoFinalSlots = {};
+    const FinalArgs<kMaxFinal>& fin = fa.final_mode ? *P.fin_slots : kNoFinalSlots;
+    ProfScope ps(h, K_FUSED, s);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = fused_config(fs.grid, s, attr);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, ns_fused_kernel<kFusedStages>, fa, fin);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return cuda_fail(h, e, "persistent Newton-Schulz launch");
+    }
+  }
+  *xk = steps & 1;
+  return MUON_OK;
+}
+
 // Failure-detection self-test: one thread waits, through the GEMMs' bounded
 // wait, on a barrier that nothing arrives at.
 __global__ void wait_selftest_kernel(int* err, uint64_t limit_ns) {
@@ -1001,6 +1362,7 @@ void muon_default_config(muon_config* cfg) {
   cfg->scale_lr_by_shape = 1;
   cfg->weight_decay = 0.0f;
   cfg->precise_carry = 0;
+  cfg->persistent = 1;
 }
 
 const char* muon_status_string(muon_status s) {
@@ -1142,12 +1504,42 @@ muon_status muon_plan_stats(const int64_t* rows, const int64_t* cols, int count,
   return MUON_OK;
 }
 
+muon_status muon_persistent_schedule(const int64_t* rows, const int64_t* cols, int count, int steps, int with_c,
+                                     int clusters, int32_t* items, int64_t items_cap, int32_t* begin,
+                                     int64_t* num_items) {
+  if (count < 0 || (count > 0 && (!rows || !cols)) || steps < 1 || steps > kFusedMaxIters || clusters < 1 ||
+      !num_items || items_cap < 0)
+    return MUON_ERR_INVALID;
+  std::vector<std::pair<int64_t, int64_t>> key(static_cast<size_t>(count));
+  for (int j = 0; j < count; ++j) {
+    if (rows[j] < 0 || cols[j] < 0) return MUON_ERR_INVALID;
+    key[j] = {rows[j], cols[j]};
+  }
+  Plan P;
+  group_shapes(key, P.mats, P.groups);
+  std::vector<int4> it;
+  std::vector<int> bg;
+  fused_schedule(P, false, steps, with_c != 0, clusters, it, bg);
+  *num_items = static_cast<int64_t>(it.size());
+  if (!items && !begin) return MUON_OK;
+  if (!items || !begin || items_cap < static_cast<int64_t>(it.size())) return MUON_ERR_INVALID;
+  for (size_t i = 0; i < it.size(); ++i) {
+    items[4 * i] = it[i].x;
+    items[4 * i + 1] = it[i].y;
+    items[4 * i + 2] = it[i].z;
+    items[4 * i + 3] = it[i].w;
+  }
+  for (size_t c = 0; c < bg.size(); ++c) begin[c] = bg[c];
+  return MUON_OK;
+}
+
 muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
   if (!out) return MUON_ERR_INVALID;
   *out = nullptr;
   if (cfg && (cfg->steps < 0 || cfg->steps > kMaxSteps || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->a) ||
               !std::isfinite(cfg->b) || !std::isfinite(cfg->c) || !(cfg->weight_decay >= 0.0f) ||
-              !std::isfinite(cfg->weight_decay) || (cfg->precise_carry != 0 && cfg->precise_carry != 1)))
+              !std::isfinite(cfg->weight_decay) || (cfg->precise_carry != 0 && cfg->precise_carry != 1) ||
+              (cfg->persistent != 0 && cfg->persistent != 1)))
     return MUON_ERR_INVALID;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
@@ -1162,8 +1554,10 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
   auto h = std::make_unique<muon_ctx>();
   h->device = device;
   h->num_sms = prop.multiProcessorCount;
+
   muon_default_config(&h->cfg);
   if (cfg) h->cfg = *cfg;
+  h->per_phase = h->cfg.persistent == 0;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
@@ -1182,10 +1576,12 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
   auto kgram = ns_gemm_kernel<true, kGramBN, kGramStages, false>;
   auto kcomb = ns_gemm_kernel<false, kCombBN, kCombStages, false>;
   auto kfinal = ns_gemm_kernel<false, kCombBN, kCombStages, true>;
+  auto kfused = ns_fused_kernel<kFusedStages>;
   cudaError_t e1 = cudaFuncSetAttribute(kgram, cudaFuncAttributeMaxDynamicSharedMemorySize, GramShape::SMEM_BYTES);
   cudaError_t e2 = cudaFuncSetAttribute(kcomb, cudaFuncAttributeMaxDynamicSharedMemorySize, CombShape::SMEM_BYTES);
   cudaError_t e3 = cudaFuncSetAttribute(kfinal, cudaFuncAttributeMaxDynamicSharedMemorySize, CombShape::SMEM_BYTES);
-  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
+  cudaError_t e4 = cudaFuncSetAttribute(kfused, cudaFuncAttributeMaxDynamicSharedMemorySize, FusedShape::SMEM_BYTES);
+  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || e4 != cudaSuccess) {
     cudaGetLastError();
     cudaFree(h->err_dev);
     return MUON_ERR_CUDA;
@@ -1200,12 +1596,16 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
     cudaLaunchConfig_t c2 = gemm_config<false, kCombBN, kCombStages>(1, nullptr, attr);
     e2 = cudaOccupancyMaxActiveClusters(&n2, kcomb, &c2);
     e3 = cudaOccupancyMaxActiveClusters(&n3, kfinal, &c2);
-    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || n1 < 1 || n2 < 1 || n3 < 1) {
+    int n4 = 0;
+    cudaLaunchConfig_t c4 = fused_config(1, nullptr, attr);
+    e4 = cudaOccupancyMaxActiveClusters(&n4, kfused, &c4);
+    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || e4 != cudaSuccess || n1 < 1 || n2 < 1 ||
+        n3 < 1 || n4 < 1) {
       cudaGetLastError();
       cudaFree(h->err_dev);
       return MUON_ERR_UNSUPPORTED;
     }
-    h->max_lists = std::min(n1, std::min(n2, n3));
+    h->max_lists = std::min(std::min(n1, n4), std::min(n2, n3));
   }
   *out = h.release();
   return MUON_OK;
@@ -1244,8 +1644,14 @@ muon_status muon_orthogonalize(muon_handle h, const muon_matrix* in, const muon_
   if ((st = launch_momentum<false>(h, *P, in, nullptr, 0.f, 0, 0, s)) != MUON_OK) return st;
   if ((st = launch_map<kScale>(h, *P, in, 0, 0.f, s, K_SCALE)) != MUON_OK) return st;
   int xk = 0;
-  const bool direct = steps >= 1 && prepare_final(h, *P, out, false, 0.f);
-  if ((st = run_iterations(h, *P, steps, a, b, c, s, &xk, direct)) != MUON_OK) return st;
+  if (h->per_phase) {
+    const bool direct = steps >= 1 && prepare_final(h, *P, out, false, 0.f);
+    if ((st = run_iterations(h, *P, steps, a, b, c, s, &xk, direct)) != MUON_OK) return st;
+    if (direct) return MUON_OK;
+    return launch_map<kCopy>(h, *P, out, xk, 0.f, s, K_COPY);
+  }
+  const bool direct = steps >= 1 && prepare_final_slots(h, *P, out, false, 0.f);
+  if ((st = run_iterations_fused(h, *P, steps, a, b, c, s, &xk, direct, false)) != MUON_OK) return st;
   if (direct) return MUON_OK;
   return launch_map<kCopy>(h, *P, out, xk, 0.f, s, K_COPY);
 }
@@ -1270,8 +1676,15 @@ muon_status muon_step(muon_handle h, const muon_matrix* params, const muon_matri
     return st;
   int xk = 0;
   // The update happens in the last combine's epilogue when the parameters allow it.
-  const bool direct = steps >= 1 && prepare_final(h, *P, params, true, lr);
-  if ((st = run_iterations(h, *P, steps, h->cfg.a, h->cfg.b, h->cfg.c, s, &xk, direct, true)) != MUON_OK)
+  if (h->per_phase) {
+    const bool direct = steps >= 1 && prepare_final(h, *P, params, true, lr);
+    if ((st = run_iterations(h, *P, steps, h->cfg.a, h->cfg.b, h->cfg.c, s, &xk, direct, true)) != MUON_OK)
+      return st;
+    if (direct) return MUON_OK;
+    return launch_map<kUpdate>(h, *P, params, xk, lr, s, K_UPDATE);
+  }
+  const bool direct = steps >= 1 && prepare_final_slots(h, *P, params, true, lr);
+  if ((st = run_iterations_fused(h, *P, steps, h->cfg.a, h->cfg.b, h->cfg.c, s, &xk, direct, true)) != MUON_OK)
     return st;
   if (direct) return MUON_OK;
   return launch_map<kUpdate>(h, *P, params, xk, lr, s, K_UPDATE);
@@ -1298,7 +1711,7 @@ muon_status muon_selftest_wait(muon_handle h, int64_t limit_ns, void* stream) {
   if (limit_ns < 1000000 || limit_ns > 2000000000) return fail(h, MUON_ERR_INVALID, "limit_ns out of [1e6, 2e9]");
   DeviceGuard guard(h->device);
   wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(h->err_dev, static_cast<uint64_t>(limit_ns));
-  return launch_checked(h, "wait self-test kernel");
+  return launch_checked(h, cudaPeekAtLastError(), "wait self-test kernel");
 }
 
 muon_status muon_set_workspace_limit(muon_handle h, int64_t bytes) {

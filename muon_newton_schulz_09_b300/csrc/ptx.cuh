@@ -141,6 +141,53 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) 
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// ---------------------------------------------------------------- flags between CTAs in global memory
+
+// Acquire load of a counter another CTA releases (gpu scope).
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Release add to a counter other CTAs acquire (gpu scope).
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Orders this thread's global-memory accesses in the generic proxy against its async-proxy (TMA)
+// accesses: after a completed TMA store, before releasing a flag; after acquiring a flag, before
+// TMA loads of what it guards.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits until *p >= target. Returns false if the CTA's abort flag is raised, or after limit_ns, in
+// which case it raises the abort flag and the kernel's error flag itself.
+__device__ __forceinline__ bool wait_counter_bounded(const int* p, int target, volatile int* abort_flag, int* err,
+                                                     uint64_t limit_ns = kWaitLimitNs) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        atomicExch(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- clusters
 
 // shared::cluster address of the variable at shared::cta address `addr` in CTA `rank` of the cluster.
