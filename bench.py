@@ -435,8 +435,10 @@ def run_ours(args) -> dict:
     w = workload_of(args.workload)
     dw = DeviceWorkload(w, local_rank)
     a, b, c = w.coeffs
-    carry = bool(getattr(args, "precise_carry", False))
-    muon = Muon(local_rank, steps=w.steps, a=a, b=b, c=c, eps=w.eps, scale_lr_by_shape=True, precise_carry=carry)
+    # The library default carries X as bf16 hi + lo exactly when c != 0; --precise-carry forces it.
+    carry = bool(getattr(args, "precise_carry", False)) or c != 0
+    muon = Muon(local_rank, steps=w.steps, a=a, b=b, c=c, eps=w.eps, scale_lr_by_shape=True,
+                precise_carry=True if getattr(args, "precise_carry", False) else None)
     stream = torch.cuda.current_stream()
     step = dw.prepared(muon, stream)
 
@@ -600,7 +602,7 @@ def run_reference(args) -> dict:
     return {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generators)",
-            "config": config_of(w, world, bool(getattr(args, "precise_carry", False))),
+            "config": config_of(w, world, bool(getattr(args, "precise_carry", False)) or w.coeffs[2] != 0),
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
@@ -709,7 +711,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=wl.GPT2_124M.name, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--precise-carry", action="store_true", help="carry X between iterations as bf16 hi + lo")
+    ap.add_argument("--precise-carry", action="store_true",
+                    help="carry X between iterations as bf16 hi + lo (the default does so only when c != 0)")
     ap.add_argument("--sharded", action="store_true",
                     help="shard whole matrices over the ranks between a reduce-scatter and an all-gather")
     args = ap.parse_args(argv)

@@ -89,21 +89,29 @@ typedef struct {
  * W <- W * (1 - lr * weight_decay) - lr * s * O. The energy-efficiency article
  * on Modded-NanoGPT (hyperparameter paragraph) reports wd = 1.0; the form is
  * this library's reading.
- * precise_carry (0 or 1): 0 rounds X to bf16 after every iteration, the stated
- * bf16 arithmetic. 1 carries X between iterations as two bf16 parts,
+ * precise_carry (0, 1 or 2): 0 rounds X to bf16 after every iteration, the
+ * stated bf16 arithmetic. 1 carries X between iterations as two bf16 parts,
  * hi = bf16(X) and lo = bf16(X - hi). The tensor cores still take hi. The
  * a*X term, X0 and the final O use hi + lo (about 16 significant bits), so
  * rounding noise does not build up over the iterations. On gradients with a
  * few dominant directions this cuts the distance to the exact iteration by
  * one to two orders of magnitude. It costs a second pair of X buffers in
  * the workspace, 4 more bytes per element in each combine pass, and combines
- * that stage their two 64-column units one after the other.
+ * that stage their two 64-column units one after the other. 2 (the default,
+ * MUON_CARRY_WHEN_C) carries X exactly for the calls whose c is nonzero
+ * (muon_step: the handle's c; muon_orthogonalize: the call's c): a quintic's
+ * slope a > 1 at zero amplifies the rounding noise that gradients with a few
+ * dominant directions put into their small singular values, and with X
+ * rounded every iteration the GPT-2 124M spiked gradients end 2.1e-2 from the
+ * exact iteration under (15, -10, 3)/8, against 5e-4 with the carry; the
+ * cubic's slope 1.5 leaves them at 8e-3 without it.
  * persistent (0 or 1): 1 runs every Newton-Schulz iteration of a call in one
  * persistent launch (up to 16 iterations per launch), whose clusters take the
  * Gram and combine tiles of all matrices from host-built work lists and wait
  * on per-matrix stage counters in global memory. 0 runs one launch per Gram
  * and per combine phase over the whole batch. Both compute the same thing
  * with the same roundings. */
+#define MUON_CARRY_WHEN_C 2
 typedef struct {
   int32_t steps;
   float a, b, c;
@@ -115,7 +123,7 @@ typedef struct {
 } muon_config;
 
 /* Fills *cfg with the defaults: steps 5, (a,b,c) = (1.5, -0.5, 0), eps 1e-7,
- * scale_lr_by_shape 1, weight_decay 0, precise_carry 0, persistent 1. The cubic coefficients
+ * scale_lr_by_shape 1, weight_decay 0, precise_carry MUON_CARRY_WHEN_C, persistent 1. The cubic coefficients
  * are the iteration's textbook form; the pages give none. */
 void muon_default_config(muon_config* cfg);
 

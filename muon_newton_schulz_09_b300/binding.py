@@ -18,6 +18,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "muon.h")
 
 MUON_OK, MUON_ERR_INVALID, MUON_ERR_CUDA, MUON_ERR_NOMEM, MUON_ERR_UNSUPPORTED, MUON_ERR_TIMEOUT = range(6)
 MUON_F32, MUON_BF16 = 0, 1
+MUON_CARRY_WHEN_C = 2
 KERNEL_KINDS = 9
 
 
@@ -220,11 +221,13 @@ class Muon:
 
     def __init__(self, device: int = 0, steps: int = 5, a: float = 1.5, b: float = -0.5, c: float = 0.0,
                  eps: float = 1e-7, scale_lr_by_shape: bool = True, weight_decay: float = 0.0,
-                 precise_carry: bool = False, persistent: bool = True):
+                 precise_carry: Optional[bool] = None, persistent: bool = True):
         self.lib = load_library()
         self.device = device
-        self.config = MuonConfig(steps, a, b, c, eps, int(bool(scale_lr_by_shape)), weight_decay,
-                                 int(bool(precise_carry)), int(bool(persistent)))
+        # precise_carry: True always, False never, None (the library default) for calls with c != 0
+        carry = MUON_CARRY_WHEN_C if precise_carry is None else int(bool(precise_carry))
+        self.config = MuonConfig(steps, a, b, c, eps, int(bool(scale_lr_by_shape)), weight_decay, carry,
+                                 int(bool(persistent)))
         h = ctypes.c_void_p()
         st = self.lib.muon_create(ctypes.byref(h), device, ctypes.byref(self.config))
         if st != MUON_OK:

@@ -176,6 +176,7 @@ struct GemmBatch {           // up to kMaxGroups groups served by one launch
 
 struct Plan {
   std::vector<std::pair<int64_t, int64_t>> key;
+  bool carry = false;  // X carried as bf16 hi + lo: low-part buffers exist and the kernels use them
   std::vector<MatInfo> mats;
   std::vector<Group> groups;
   std::vector<GemmBatch> batches;
@@ -225,7 +226,8 @@ struct muon_ctx {
   int* err_dev = nullptr;            // 256 bytes: the error flag at 0, the profiling clock sums at 64
   unsigned long long* clk_dev = nullptr;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  std::map<std::vector<std::pair<int64_t, int64_t>>, std::unique_ptr<Plan>> plans;
+  // Plans by (matrix shapes, precise carry).
+  std::map<std::pair<std::vector<std::pair<int64_t, int64_t>>, bool>, std::unique_ptr<Plan>> plans;
   uint64_t use_clock = 0;
   std::string last_error;
   // profiling
@@ -440,10 +442,11 @@ cudaError_t plan_malloc(muon_handle h, Plan& P, void** ptr, size_t bytes) {
   return e;
 }
 
-muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t>>& key, Plan** out) {
+muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t>>& key, bool carry, Plan** out) {
   auto plan = std::make_unique<Plan>();
   Plan& P = *plan;
   P.key = key;
+  P.carry = carry;
   group_shapes(key, P.mats, P.groups);
 
   // Workspace: per group X ping/pong [count][n][ld_x], B and A [count][n][ld_p];
@@ -461,7 +464,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
     g.x_off[1] = take(xb);
     g.p_off = take(pb);
     g.a_off = take(pb);
-    if (h->cfg.precise_carry) {
+    if (P.carry) {
       g.lo_off[0] = take(xb);
       g.lo_off[1] = take(xb);
     }
@@ -596,7 +599,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
         B.comb[t].grp[gi] = GemmGroup{reinterpret_cast<uint16_t*>(xb[t]), nullptr, g.n * g.ld_x, static_cast<int>(g.n),
                                       static_cast<int>(g.m), static_cast<int>(g.ld_x),
                                       static_cast<int>(ceil_div(g.n, 64))};
-        if (h->cfg.precise_carry) {  // addend and output low parts, laid out like X
+        if (P.carry) {  // addend and output low parts, laid out like X
           uint8_t* lb[2] = {P.ws + g.lo_off[0], P.ws + g.lo_off[1]};
           ok &= encode_map(h, &B.comb[t].map_e_lo[gi], lb[t], g.m, g.n, g.count, g.ld_x, 64, 128);
           ok &= encode_map(h, &B.comb[t].map_out_lo[gi], lb[1 - t], g.m, g.n, g.count, g.ld_x, 64, 128);
@@ -634,7 +637,7 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
         ok &= encode_map(h, &m[kRoleX0 + t], xb[t], g.m, g.n, g.count, g.ld_x, 64, 128);
         ok &= encode_map(h, &m[kRoleXmn0 + t], xb[t], g.m, g.n, g.count, g.ld_x, 64, 64);
         // Without the precise carry the low-part roles are never used; they hold valid maps of X.
-        uint8_t* lb = h->cfg.precise_carry ? P.ws + g.lo_off[t] : xb[t];
+        uint8_t* lb = P.carry ? P.ws + g.lo_off[t] : xb[t];
         ok &= encode_map(h, &m[kRoleLo0 + t], lb, g.m, g.n, g.count, g.ld_x, 64, 128);
       }
       ok &= encode_map(h, &m[kRoleP], pbuf, g.n, g.n, g.count, g.ld_p, 64, 128);
@@ -671,12 +674,12 @@ muon_status build_plan(muon_handle h, const std::vector<std::pair<int64_t, int64
     return cuda_fail(h, e, "plan synchronize");
   }
   *out = plan.get();
-  h->plans[key] = std::move(plan);
+  h->plans[std::make_pair(key, carry)] = std::move(plan);
   return MUON_OK;
 }
 
-muon_status get_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t>>& key, Plan** out) {
-  auto it = h->plans.find(key);
+muon_status get_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t>>& key, bool carry, Plan** out) {
+  auto it = h->plans.find(std::make_pair(key, carry));
   if (it != h->plans.end()) {
     it->second->last_use = ++h->use_clock;
     *out = it->second.get();
@@ -690,7 +693,7 @@ muon_status get_plan(muon_handle h, const std::vector<std::pair<int64_t, int64_t
     free_plan(h, victim->second.get());
     h->plans.erase(victim);
   }
-  muon_status s = build_plan(h, key, out);
+  muon_status s = build_plan(h, key, carry, out);
   if (s == MUON_OK) (*out)->last_use = ++h->use_clock;
   return s;
 }
@@ -1261,7 +1264,7 @@ muon_status run_iterations_fused(muon_handle h, Plan& P, int steps, float a, flo
     if (it == P.fused.end()) {
       std::vector<int4> items;
       std::vector<int> begin;
-      fused_schedule(P, h->cfg.precise_carry != 0, iters, c_nz, h->max_lists, items, begin);
+      fused_schedule(P, P.carry, iters, c_nz, h->max_lists, items, begin);
       Plan::FusedSchedule fs;
       fs.grid = static_cast<int>(begin.size()) - 1;
       const size_t ib = items.size() * sizeof(int4), bb = begin.size() * sizeof(int);
@@ -1300,7 +1303,7 @@ muon_status run_iterations_fused(muon_handle h, Plan& P, int steps, float a, flo
     fa.a = a;
     fa.b = b;
     fa.c = c;
-    fa.carry = h->cfg.precise_carry ? 1 : 0;
+    fa.carry = P.carry ? 1 : 0;
     fa.final_mode = (final_into_user && i0 + iters == steps) ? 1 : 0;
     fa.err = h->err_dev;
     fa.clk = h->profiling ? h->clk_dev : nullptr;
@@ -1340,6 +1343,11 @@ std::vector<std::pair<int64_t, int64_t>> shape_key(const muon_matrix* m, int cou
   return k;
 }
 
+// Whether a call with coefficient c carries X as bf16 hi + lo (muon_config.precise_carry).
+bool uses_carry(const muon_config& cfg, float c) {
+  return cfg.precise_carry == 1 || (cfg.precise_carry == MUON_CARRY_WHEN_C && c != 0.0f);
+}
+
 bool all_skipped(const muon_matrix* m, int count) {
   for (int j = 0; j < count; ++j)
     if (m[j].rows > 0 && m[j].cols > 0) return false;
@@ -1361,7 +1369,7 @@ void muon_default_config(muon_config* cfg) {
   cfg->eps = 1e-7f;
   cfg->scale_lr_by_shape = 1;
   cfg->weight_decay = 0.0f;
-  cfg->precise_carry = 0;
+  cfg->precise_carry = MUON_CARRY_WHEN_C;
   cfg->persistent = 1;
 }
 
@@ -1538,7 +1546,7 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
   *out = nullptr;
   if (cfg && (cfg->steps < 0 || cfg->steps > kMaxSteps || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->a) ||
               !std::isfinite(cfg->b) || !std::isfinite(cfg->c) || !(cfg->weight_decay >= 0.0f) ||
-              !std::isfinite(cfg->weight_decay) || (cfg->precise_carry != 0 && cfg->precise_carry != 1) ||
+              !std::isfinite(cfg->weight_decay) || (cfg->precise_carry < 0 || cfg->precise_carry > 2) ||
               (cfg->persistent != 0 && cfg->persistent != 1)))
     return MUON_ERR_INVALID;
   int ndev = 0;
@@ -1640,7 +1648,7 @@ muon_status muon_orthogonalize(muon_handle h, const muon_matrix* in, const muon_
   DeviceGuard guard(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Plan* P = nullptr;
-  if ((st = get_plan(h, shape_key(in, count), &P)) != MUON_OK) return st;
+  if ((st = get_plan(h, shape_key(in, count), uses_carry(h->cfg, c), &P)) != MUON_OK) return st;
   if ((st = launch_momentum<false>(h, *P, in, nullptr, 0.f, 0, 0, s)) != MUON_OK) return st;
   if ((st = launch_map<kScale>(h, *P, in, 0, 0.f, s, K_SCALE)) != MUON_OK) return st;
   int xk = 0;
@@ -1667,7 +1675,7 @@ muon_status muon_step(muon_handle h, const muon_matrix* params, const muon_matri
   DeviceGuard guard(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Plan* P = nullptr;
-  if ((st = get_plan(h, shape_key(params, count), &P)) != MUON_OK) return st;
+  if ((st = get_plan(h, shape_key(params, count), uses_carry(h->cfg, h->cfg.c), &P)) != MUON_OK) return st;
   // u goes into the first X buffer unscaled; its 1/(||u||_F + eps) is folded into the first
   // iteration's Gram and combine, except for norms outside the safe range, where the momentum
   // kernel scales u in place (and always with zero iterations).

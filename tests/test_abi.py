@@ -28,7 +28,7 @@ def test_default_config():
     cfg = mu.MuonConfig()
     mu.load_library().muon_default_config(ctypes.byref(cfg))
     assert (cfg.steps, cfg.a, cfg.b, cfg.c, cfg.scale_lr_by_shape, cfg.weight_decay, cfg.precise_carry,
-            cfg.persistent) == (5, 1.5, -0.5, 0.0, 1, 0.0, 0, 1)
+            cfg.persistent) == (5, 1.5, -0.5, 0.0, 1, 0.0, 2, 1)
     assert abs(cfg.eps - 1e-7) < 1e-12
 
 
@@ -129,7 +129,7 @@ def test_profiling_calls_reject_a_null_handle():
 def test_create_rejects_a_bad_config_before_touching_a_gpu():
     lib = mu.load_library()
     h = ctypes.c_void_p()
-    for field, value in [("precise_carry", 2), ("steps", -1), ("weight_decay", -0.5), ("eps", float("nan")),
+    for field, value in [("precise_carry", 3), ("precise_carry", -1), ("steps", -1), ("weight_decay", -0.5), ("eps", float("nan")),
                          ("persistent", 3)]:
         cfg = mu.MuonConfig()
         lib.muon_default_config(ctypes.byref(cfg))

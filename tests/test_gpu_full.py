@@ -65,27 +65,18 @@ def test_gpt2_350m_full_step(muon):
 
 
 def test_gpt2_124m_quintic_step():
-    """The c != 0 path (an A A Gram pass with b A in its epilogue) in the benchmark's launch configuration."""
+    """The c != 0 path (an A A Gram pass with b A in its epilogue) in the benchmark's launch
+    configuration, on the spiked GPT-2 124M gradients, with the default config: calls with c != 0
+    carry X as bf16 hi + lo, which keeps this case well inside the bar (X rounded to bf16 every
+    iteration ends about 2.1e-2 from the exact iteration here)."""
     from muon_newton_schulz_09_b300 import Muon
     w = wl.GPT2_124M_QUINTIC
+    assert w.spike_rank == 4
     a, b, c = w.coeffs
     with Muon(0, steps=w.steps, a=a, b=b, c=c) as mq:
         errs = _step_check(mq, w, sample=[0, 4, 5, 71])
-    print("gpt2_124m quintic rel-F per sampled matrix:", errs)
-
-
-def test_gpt2_124m_spiked_quintic_precise_carry():
-    """The spiked GPT-2 124M gradients with the quintic: with X rounded to bf16 every iteration this
-    case ends about 2.1e-2 from the exact iteration (any bf16 evaluation does). Carrying X as
-    bf16 hi + lo brings it well inside the bar."""
-    import dataclasses
-    from muon_newton_schulz_09_b300 import Muon
-    w = dataclasses.replace(wl.GPT2_124M_QUINTIC, name="gpt2_124m_spiked_quintic", spike_rank=4, spike_gain=50.0)
-    a, b, c = w.coeffs
-    with Muon(0, steps=w.steps, a=a, b=b, c=c, precise_carry=True) as mq:
-        errs = _step_check(mq, w, sample=[0, 4, 5, 71])
     assert max(errs.values()) < 5e-3, errs
-    print("gpt2_124m spiked quintic, precise carry, rel-F per sampled matrix:", errs)
+    print("gpt2_124m spiked quintic rel-F per sampled matrix:", errs)
 
 
 def test_square_64x1024(muon):

@@ -149,15 +149,16 @@ GPT2_350M = Workload(
     grad_std=1e-3, seed=5,
     notes="24 x (4x 1024^2, 1024x4096, 4096x1024) bf16, N(0,1e-3), full step incl. update")
 
-# The c != 0 path at benchmark scale: the GPT-2 124M set with the second-order Newton-Schulz
-# quintic (15, -10, 3)/8 (the pages give no coefficients; this is the textbook polynomial).
-# No spike: with the rank-4 spike, bf16 rounding noise of the spike directions lands in the
-# tiny bulk singular values and the quintic's slope 15/8 at zero amplifies it 15/8 per
-# iteration, so any bf16 evaluation ends about 2.1e-2 from the exact result there.
+# The c != 0 path at benchmark scale: the GPT-2 124M set, its gradients with the rank-4 spike,
+# and the second-order Newton-Schulz quintic (15, -10, 3)/8 (the pages give no coefficients; this
+# is the textbook polynomial). The spike's bf16 rounding noise lands in the tiny bulk singular
+# values and the quintic's slope 15/8 at zero amplifies it every iteration: X rounded to bf16
+# every iteration ends about 2.1e-2 from the exact result, so calls with c != 0 carry X as
+# bf16 hi + lo by default.
 GPT2_124M_QUINTIC = Workload(
     name="gpt2_124m_hidden_quintic", shapes=_gpt2_shapes(12, 768), kind="step", dtype="bf16",
-    grad_std=1e-3, seed=2, coeffs=(15 / 8, -10 / 8, 3 / 8),
-    notes="GPT-2 124M hidden set, N(0,1e-3) gradients, quintic (15,-10,3)/8 Newton-Schulz, 5 iterations")
+    grad_std=1e-3, spike_rank=4, spike_gain=50.0, seed=2, coeffs=(15 / 8, -10 / 8, 3 / 8),
+    notes="GPT-2 124M hidden set, N(0,1e-3) + rank-4 spike x50, quintic (15,-10,3)/8 Newton-Schulz, 5 iterations")
 
 WORKLOADS = {w.name: w for w in (SINGLE_128x256, GPT2_124M, SQUARE_64x1024, ILLCOND_4096x16384, GPT2_350M,
                                  GPT2_124M_QUINTIC)}
