@@ -42,13 +42,14 @@ SMS = 148
 # by the hash of the kernel sources' code (comments excluded) they were taken with. A stale
 # hash gives null.
 NCU_TRAFFIC = {
-    # ncu --set full on the GPT-2 124M set (the A A pass on its quintic variant). The combine kind
-    # averages its launches, so its figure is (4 x 389.4 MB + 556.5 MB for the last, fused one) / 5.
-    "df6eae1de82e8e6d": {"gram_xxt": 211.3e6, "combine_ax_bx": 422.8e6, "gram_aa": 127.3e6},
+    # ncu --set full on the GPT-2 124M step: the persistent launch running all 5 iterations
+    # (profiles/persistent_ns_gpt2_124m.md), 2.118 GB read + 1.245 GB written.
+    "b9482563b7d09cb8": {"newton_schulz": 3.363e9},
 }
 
 KERNEL_SOURCES = ["muon_newton_schulz_09_b300/csrc/ns_gemm.cuh", "muon_newton_schulz_09_b300/csrc/elementwise.cuh",
-                  "muon_newton_schulz_09_b300/csrc/ptx.cuh", "muon_newton_schulz_09_b300/csrc/muon_api.cu"]
+                  "muon_newton_schulz_09_b300/csrc/ptx.cuh", "muon_newton_schulz_09_b300/csrc/muon_api.cu",
+                  "muon_newton_schulz_09_b300/csrc/ns_fused.cuh"]
 
 
 def code_text(src: str) -> str:
