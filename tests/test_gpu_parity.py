@@ -522,3 +522,52 @@ def test_per_phase_launches_match_the_oracle(coeffs, steps):
         upd = lr * oracle.lr_scale(r, c) * np.abs(o).max()
         err = np.abs(host(P[j]) - w_new)
         assert np.all(err <= bf16_ulp(w_new) + 0.05 * upd), (r, c, float(err.max()))
+
+
+def test_persistent_and_per_phase_launches_agree_bit_for_bit():
+    """The persistent launch and the per-phase launches run the same tiles with the same arithmetic, so
+    their outputs are equal bit for bit: orthogonalize (cubic, and the quintic with its default
+    carry) on the ragged batch, and a step whose last combine writes bf16 parameters."""
+    from muon_newton_schulz_09_b300 import Muon
+    _, xs = inputs_for(RAGGED, "bf16", seed=13)
+    shapes = [(256, 640), (640, 256), (130, 70), (1, 5)]
+    w, g, m, p = step_case(shapes, "bf16", "bf16", seed=30)
+    outs = {}
+    for persistent in (True, False):
+        with Muon(0, persistent=persistent) as mu:
+            o1 = run_orth(mu, xs, "bf16", "f32", 5, CUBIC)
+            o2 = run_orth(mu, xs, "bf16", "bf16", 3, QUINTIC)
+            P = [dev(x, "bf16") for x in p]
+            M = [dev(x, "f32") for x in m]
+            mu.step(P, [dev(x, "bf16") for x in g], M, lr=0.02, beta=0.95, nesterov=True)
+            torch.cuda.synchronize()
+            assert mu.get_error() == 0
+            outs[persistent] = (o1, o2, [host(t) for t in P], [host(t) for t in M])
+    for a, b in zip(outs[True], outs[False]):
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
+
+
+def test_quintic_over_several_persistent_launches():
+    """20 quintic iterations take two persistent launches (16 + 4): the second starts from the first's
+    X, the folded scale applies only in the first and the update only in the last. The default config
+    carries X as hi + lo for c != 0 across both."""
+    from muon_newton_schulz_09_b300 import Muon
+    shapes = [(256, 640), (640, 256), (130, 70), (384, 384)]
+    w, g, m, p = step_case(shapes, "bf16", "bf16", seed=31)
+    lr, steps = 0.02, 20
+    with Muon(0, steps=steps, a=QUINTIC[0], b=QUINTIC[1], c=QUINTIC[2]) as mq:
+        mq.profile_read()
+        mq.profile(True)
+        P = [dev(x, "bf16") for x in p]
+        mq.step(P, [dev(x, "bf16") for x in g], [dev(x, "f32") for x in m], lr=lr, beta=0.95, nesterov=True)
+        torch.cuda.synchronize()
+        mq.profile(False)
+        prof = mq.profile_read()
+        assert mq.get_error() == 0
+        assert prof["newton_schulz"][1] == 2
+    for j, (r, c) in enumerate(shapes):
+        w_new, _, o = oracle.muon_step(p[j], g[j], m[j], lr, 0.95, True, steps, QUINTIC)
+        upd = lr * oracle.lr_scale(r, c) * np.abs(o).max()
+        err = np.abs(host(P[j]) - w_new)
+        assert np.all(err <= bf16_ulp(w_new) + 0.05 * upd), (r, c, float(err.max()))
