@@ -231,7 +231,9 @@ muon_status muon_workspace_bytes(muon_handle h, int64_t* bytes);
  * group (groups are the distinct oriented shapes, in order of first
  * appearance), tile row | tile column << 16, and the number of finished
  * epilogue halves (four per tile) of the matrix the item waits for. Cluster c
- * takes items[begin[c] .. begin[c+1]) in order. Writes the item count to
+ * takes items[begin[c] .. begin[c+1]) in order. More than 1024 distinct
+ * oriented shapes give MUON_ERR_UNSUPPORTED (such calls run the per-phase
+ * launches whatever muon_config.persistent says). Writes the item count to
  * *num_items; with items and begin NULL nothing else is written, otherwise
  * items needs room for 4 * *num_items values and begin for clusters + 1. */
 muon_status muon_persistent_schedule(const int64_t* rows, const int64_t* cols, int count, int steps, int with_c,
@@ -245,6 +247,18 @@ muon_status muon_persistent_schedule(const int64_t* rows, const int64_t* cols, i
  * flag and returns, so the next muon_get_error reports MUON_ERR_TIMEOUT and
  * the context stays usable. Nothing traps or faults. */
 muon_status muon_selftest_wait(muon_handle h, int64_t limit_ns, void* stream);
+
+/* Failure-detection self-test of the persistent Newton-Schulz launch
+ * (muon_config.persistent): one launch over a 256 x 256 matrix of the
+ * handle's workspace whose first work item waits for a stage count its matrix
+ * never reaches. Every wait of that launch gives up after limit_ns (1e6 ..
+ * 2e9 ns, else MUON_ERR_INVALID); the CTAs that gave up stop, let their
+ * copies and MMAs in flight land and free their tensor memory, the last one
+ * resets the stage counters, and the device error flag is raised, so the next
+ * muon_get_error reports MUON_ERR_TIMEOUT and later calls run normally.
+ * Nothing traps or faults. The call waits for the launch (a few limit_ns at
+ * most); the caller's tensors are not touched. */
+muon_status muon_selftest_persistent(muon_handle h, int64_t limit_ns, void* stream);
 
 /* Kernel timing, for benchmarks. While enabled, each kernel the handle
  * launches is bracketed by CUDA events on the launching stream.

@@ -79,6 +79,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "muon_profile_clock": (c.c_int, [c.c_void_p, P(c.c_double)]),
         "muon_kernel_name": (c.c_char_p, [c.c_int]),
         "muon_selftest_wait": (c.c_int, [c.c_void_p, c.c_int64, c.c_void_p]),
+        "muon_selftest_persistent": (c.c_int, [c.c_void_p, c.c_int64, c.c_void_p]),
         "muon_set_workspace_limit": (c.c_int, [c.c_void_p, c.c_int64]),
         "muon_persistent_schedule": (c.c_int, [P(c.c_int64), P(c.c_int64), c.c_int, c.c_int, c.c_int, c.c_int,
                                                P(c.c_int32), c.c_int64, P(c.c_int32), P(c.c_int64)]),
@@ -301,6 +302,11 @@ class Muon:
         v = ctypes.c_int64()
         self._check(self.lib.muon_workspace_bytes(self.handle, ctypes.byref(v)), "muon_workspace_bytes")
         return v.value
+
+    def selftest_persistent(self, limit_ns: int = 50_000_000, stream=None):
+        """Runs the persistent launch's failure-detection self-test (a stage wait that must expire)."""
+        self._check(self.lib.muon_selftest_persistent(self.handle, int(limit_ns), _stream_ptr(stream, self.device)),
+                    "muon_selftest_persistent")
 
     def get_error(self, stream=None) -> int:
         return self.lib.muon_get_error(self.handle, _stream_ptr(stream, self.device))

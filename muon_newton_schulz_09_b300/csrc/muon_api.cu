@@ -1054,6 +1054,8 @@ muon_status run_iterations(muon_handle h, const Plan& P, int steps, float a, flo
 // Iterations one persistent launch covers at most; longer runs take several launches. Even, so every
 // launch starts with X in buffer 0 or an even iteration's buffer, as its items assume.
 constexpr int kFusedMaxIters = 16;
+// Shape groups one persistent launch can name (10 bits of a work item); more take the per-phase launches.
+constexpr size_t kFusedMaxGroups = 1024;
 
 struct SimMatrix {
   int slot = 0;
@@ -1525,6 +1527,7 @@ muon_status muon_persistent_schedule(const int64_t* rows, const int64_t* cols, i
   }
   Plan P;
   group_shapes(key, P.mats, P.groups);
+  if (P.groups.size() > kFusedMaxGroups) return MUON_ERR_UNSUPPORTED;
   std::vector<int4> it;
   std::vector<int> bg;
   fused_schedule(P, false, steps, with_c != 0, clusters, it, bg);
@@ -1652,7 +1655,7 @@ muon_status muon_orthogonalize(muon_handle h, const muon_matrix* in, const muon_
   if ((st = launch_momentum<false>(h, *P, in, nullptr, 0.f, 0, 0, s)) != MUON_OK) return st;
   if ((st = launch_map<kScale>(h, *P, in, 0, 0.f, s, K_SCALE)) != MUON_OK) return st;
   int xk = 0;
-  if (h->per_phase) {
+  if (h->per_phase || P->groups.size() > kFusedMaxGroups) {
     const bool direct = steps >= 1 && prepare_final(h, *P, out, false, 0.f);
     if ((st = run_iterations(h, *P, steps, a, b, c, s, &xk, direct)) != MUON_OK) return st;
     if (direct) return MUON_OK;
@@ -1684,7 +1687,7 @@ muon_status muon_step(muon_handle h, const muon_matrix* params, const muon_matri
     return st;
   int xk = 0;
   // The update happens in the last combine's epilogue when the parameters allow it.
-  if (h->per_phase) {
+  if (h->per_phase || P->groups.size() > kFusedMaxGroups) {
     const bool direct = steps >= 1 && prepare_final(h, *P, params, true, lr);
     if ((st = run_iterations(h, *P, steps, h->cfg.a, h->cfg.b, h->cfg.c, s, &xk, direct, true)) != MUON_OK)
       return st;
@@ -1720,6 +1723,60 @@ muon_status muon_selftest_wait(muon_handle h, int64_t limit_ns, void* stream) {
   DeviceGuard guard(h->device);
   wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(h->err_dev, static_cast<uint64_t>(limit_ns));
   return launch_checked(h, cudaPeekAtLastError(), "wait self-test kernel");
+}
+
+muon_status muon_selftest_persistent(muon_handle h, int64_t limit_ns, void* stream) {
+  if (!h) return MUON_ERR_INVALID;
+  if (limit_ns < 1000000 || limit_ns > 2000000000) return fail(h, MUON_ERR_INVALID, "limit_ns out of [1e6, 2e9]");
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // One 256 x 256 matrix, one iteration, with the first item of the first list waiting for a stage
+  // count its matrix never reaches.
+  Plan* P = nullptr;
+  muon_status st = get_plan(h, {{256, 256}}, false, &P);
+  if (st != MUON_OK) return st;
+  std::vector<int4> items;
+  std::vector<int> begin;
+  fused_schedule(*P, false, 1, false, h->max_lists, items, begin);
+  if (items.empty()) return fail(h, MUON_ERR_CUDA, "empty self-test schedule");
+  items[begin[0]].w = 1 << 30;
+  const size_t ib = items.size() * sizeof(int4), bb = begin.size() * sizeof(int);
+  void* buf = nullptr;
+  cudaError_t e = cudaMalloc(&buf, ib + bb);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(h, MUON_ERR_NOMEM, "self-test schedule: %s", cudaGetErrorString(e));
+  }
+  e = cudaMemcpy(buf, items.data(), ib, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(static_cast<uint8_t*>(buf) + ib, begin.data(), bb, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) {
+    FusedArgs fa;
+    memset(&fa, 0, sizeof(fa));
+    fa.maps = P->maps_dev;
+    fa.groups = P->groups_dev;
+    fa.items = static_cast<int4*>(buf);
+    fa.begin = reinterpret_cast<int*>(static_cast<uint8_t*>(buf) + ib);
+    fa.counters = P->counters;
+    fa.done = P->done;
+    fa.num_slots = 1;
+    fa.num_groups = static_cast<int>(P->groups.size());
+    fa.a = 1.5f;
+    fa.b = -0.5f;
+    fa.err = h->err_dev;
+    fa.wait_ns = static_cast<uint64_t>(limit_ns);
+    static const FinalArgs<kMaxFinal> kNone = {};
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = fused_config(static_cast<int>(begin.size()) - 1, s, attr);
+    e = cudaLaunchKernelEx(&cfg, ns_fused_kernel<kFusedStages>, fa, kNone);
+    // The schedule buffer must outlive the launch; this call waits for it.
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  cudaFree(buf);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(h, e, "persistent self-test");
+  }
+  return MUON_OK;
 }
 
 muon_status muon_set_workspace_limit(muon_handle h, int64_t bytes) {

@@ -81,6 +81,7 @@ struct FusedArgs {
   int final_mode;            // 1: the last combine writes the caller's matrices through `fin`
   int* err;
   unsigned long long* clk;
+  uint64_t wait_ns;          // limit of every bounded wait (0: kWaitLimitNs); the self-test shortens it
 };
 
 template <int kStages>
@@ -111,6 +112,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int rank = static_cast<int>(cluster_cta_rank());
   const int list = blockIdx.x / kCluster;
   const int t_begin = args.begin[list], t_end = args.begin[list + 1];
+  const uint64_t lim = args.wait_ns ? args.wait_ns : kWaitLimitNs;
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int st) { return bar0 + 8u * st; };
   auto empty_bar = [&](int st) { return bar0 + 8u * (kStages + st); };
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int kind = it.x & 3, g = (it.x >> 2) & 1023, flags = it.x >> 12;
         const int I = (it.z & 0xFFFF) + rank, J = it.z >> 16;
         const NsGroup G = args.groups[g];
-        if (it.w > 0 && !wait_counter_bounded(args.counters + G.first_slot + it.y, it.w, abort_flag, args.err))
+        if (it.w > 0 && !wait_counter_bounded(args.counters + G.first_slot + it.y, it.w, abort_flag, args.err, lim))
           break;
         fence_proxy_async_global();
         const bool gram = kind != kNsComb;
@@ -182,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t bytes = a_in_b ? B_BYTES : A_BYTES + B_BYTES;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err, lim)) {
             ok = false;
             break;
           }
@@ -227,12 +229,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int nk = kind == kNsGram ? args.groups[g].nk_m : args.groups[g].nk_n;
         const bool a_in_b = gram && ((I >> 1) == J);
         const uint32_t idesc = gram ? kIdescK : kIdescMN;
-        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err)) break;
+        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err, lim)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.err)) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.err, lim)) {
             ok = false;
             break;
           }
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       box_pending |= 1u << b;
     };
     auto wait_box = [&](int b) -> bool {
-      if (!mbar_wait_bounded(box_bar(b), (box_phase >> b) & 1u, abort_flag, args.err)) return false;
+      if (!mbar_wait_bounded(box_bar(b), (box_phase >> b) & 1u, abort_flag, args.err, lim)) return false;
       box_phase ^= 1u << b;
       box_pending &= ~(1u << b);
       return true;
@@ -350,7 +352,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool final_out = !gram && (flags & kNsLast) && args.final_mode;
       // The stage this item's addend comes from has finished once the item's dependency holds.
       if (has_e && it.w > 0 && leader) {
-        if (wait_counter_bounded(args.counters + slot, it.w, abort_flag, args.err)) fence_proxy_async_global();
+        if (wait_counter_bounded(args.counters + slot, it.w, abort_flag, args.err, lim)) fence_proxy_async_global();
       }
       const CUtensorMap* m_out;
       const CUtensorMap* m_mirror = nullptr;
@@ -395,7 +397,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           load_box(1, m_e, col_base + 64, y_tile, mat, true);
         }
       }
-      mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err);
+      mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, lim);
       tc_fence_after();
       bool released = false;
       if (carry && !skip) {

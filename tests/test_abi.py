@@ -116,6 +116,7 @@ def test_plan_stats_ragged_and_c():
 def test_selftest_wait_rejects_bad_limits_without_a_handle():
     lib = mu.load_library()
     assert lib.muon_selftest_wait(None, 50_000_000, None) == MUON_ERR_INVALID
+    assert lib.muon_selftest_persistent(None, 50_000_000, None) == MUON_ERR_INVALID
 
 
 def test_profiling_calls_reject_a_null_handle():

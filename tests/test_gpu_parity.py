@@ -276,6 +276,24 @@ def test_bounded_wait_expiry_is_reported_and_recoverable(muon):
     assert rel_f(got[0], oracle.orthogonalize(xs[0], 5, CUBIC)) < TOL
 
 
+def test_persistent_stage_wait_expiry_is_reported_and_recoverable(muon):
+    """The persistent launch with a planted work item whose stage count is never reached: every wait
+    gives up after 50 ms, the launch ends with MUON_ERR_TIMEOUT instead of hanging or faulting, the
+    stage counters are reset, and the same plan then computes the right result."""
+    import time
+    from muon_newton_schulz_09_b300 import MUON_ERR_TIMEOUT, MUON_OK
+    assert muon.get_error() == MUON_OK
+    t0 = time.perf_counter()
+    muon.selftest_persistent(50_000_000)
+    elapsed = time.perf_counter() - t0
+    assert muon.get_error() == MUON_ERR_TIMEOUT
+    assert elapsed < 5.0, elapsed
+    _, xs = inputs_for([(256, 256)], "bf16", seed=48)
+    got = run_orth(muon, xs, "bf16", "f32", 5, CUBIC)  # the self-test's plan, counters reset
+    assert muon.get_error() == MUON_OK
+    assert rel_f(got[0], oracle.orthogonalize(xs[0], 5, CUBIC)) < TOL
+
+
 def test_profiling_counts_launches_and_reads_the_sm_clock(muon):
     """Profiling brackets each kernel with events and has the GEMM kernels report their own SM clock."""
     _, xs = inputs_for([(256, 384), (384, 256)], "bf16", seed=17)
@@ -571,3 +589,14 @@ def test_quintic_over_several_persistent_launches():
         upd = lr * oracle.lr_scale(r, c) * np.abs(o).max()
         err = np.abs(host(P[j]) - w_new)
         assert np.all(err <= bf16_ulp(w_new) + 0.05 * upd), (r, c, float(err.max()))
+
+
+def test_more_shape_groups_than_the_persistent_launch_names():
+    """1025 distinct shapes (1 x k rows): the call runs the per-phase launches and is still right."""
+    shapes = [(1, k) for k in range(1, 1026)]
+    _, xs = inputs_for(shapes, "bf16", seed=47)
+    from muon_newton_schulz_09_b300 import Muon
+    with Muon(0) as mu:
+        got = run_orth(mu, xs, "bf16", "f32", 5, CUBIC)
+    for j in (0, 1, 511, 1024):
+        assert rel_f(got[j], oracle.orthogonalize(xs[j], 5, CUBIC)) < TOL, shapes[j]

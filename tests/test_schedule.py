@@ -129,3 +129,13 @@ def test_bad_arguments_are_rejected():
     for steps, clusters in [(0, 4), (17, 4), (2, 0)]:
         with pytest.raises(MuonError):
             persistent_schedule([(64, 64)], steps, False, clusters)
+
+
+def test_more_shape_groups_than_an_item_can_name_is_refused():
+    """A work item names its shape group in 10 bits; 1025 distinct shapes are refused here, and the
+    library runs such calls with the per-phase launches instead."""
+    from muon_newton_schulz_09_b300 import MuonError, MUON_ERR_UNSUPPORTED
+    persistent_schedule([(1, k) for k in range(1, 1025)], 1, False, 4)
+    with pytest.raises(MuonError) as e:
+        persistent_schedule([(1, k) for k in range(1, 1026)], 1, False, 4)
+    assert e.value.status == MUON_ERR_UNSUPPORTED
