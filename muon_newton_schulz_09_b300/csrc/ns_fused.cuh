@@ -418,6 +418,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[cc * 32 + k] = s_acc * __uint_as_float(r[k]);
           }
+          if (box == kBoxes - 1) {  // the whole accumulator is read: hand it back before the addend wait
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+            released = true;
+          }
           add_carried_addend(v, s_e);
           uint8_t* rh = stg_box(0) + (quarter * 32 + lane) * 128;
           uint8_t* rl = stg_box(1) + (quarter * 32 + lane) * 128;
@@ -572,6 +578,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tmem_load_wait();
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[cc * 32 + k] = s_acc * __uint_as_float(r[k]);
+          }
+          if (box == kBoxes - 1) {  // the whole accumulator is read: hand it back before the stores
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+            released = true;
           }
           const int x0 = col_base + box * 64;
           const int b = has_e ? box : (ring & 1);
