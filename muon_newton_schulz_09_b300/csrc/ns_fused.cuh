@@ -633,8 +633,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      sync_half();
-      if (*abort_flag) break;
+      // Every warp of the half takes the same decision: one that read the flag before another thread
+      // raised it would otherwise go on alone and wait at the next named barrier for ever.
+      if (named_barrier_or(half_bar, 128, *abort_flag != 0)) break;
       if (!released) {
         tc_fence_before();
         __syncwarp();

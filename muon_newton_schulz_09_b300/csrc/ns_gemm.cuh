@@ -672,8 +672,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      sync_half();  // the abort flag, if raised in this tile, is seen by all four warps alike
-      if (*abort_flag) break;
+      // All four warps take the same decision, even when another warp raises the flag between their reads.
+      if (named_barrier_or(half_bar, 128, *abort_flag != 0)) break;
       if (!released) {
         tc_fence_before();
         __syncwarp();
