@@ -105,13 +105,20 @@ typedef struct {
  * rounded every iteration the GPT-2 124M spiked gradients end 2.1e-2 from the
  * exact iteration under (15, -10, 3)/8, against 5e-4 with the carry; the
  * cubic's slope 1.5 leaves them at 8e-3 without it.
- * persistent (0 or 1): 1 runs every Newton-Schulz iteration of a call in one
- * persistent launch (up to 16 iterations per launch), whose clusters take the
- * Gram and combine tiles of all matrices from host-built work lists and wait
- * on per-matrix stage counters in global memory. 0 runs one launch per Gram
- * and per combine phase over the whole batch. Both compute the same thing
- * with the same roundings. */
+ * persistent (0, 1 or 2): 1 runs every Newton-Schulz iteration of a call in
+ * one persistent launch (up to 16 iterations per launch), whose clusters take
+ * the Gram and combine tiles of all matrices from host-built work lists and
+ * wait on per-matrix stage counters in global memory. 0 runs one launch per
+ * Gram and per combine phase over the whole batch. 2 (the default,
+ * MUON_PERSISTENT_AUTO) chooses per call: the per-phase launches when one
+ * iteration gives every resident 2-CTA cluster 800 or more 64-wide k-blocks
+ * of 256 x 256 tiles (each phase then streams enough tiles that its ramp and
+ * tail cost less than the persistent launch's item changes), the persistent
+ * launch otherwise (muon_launch_choice reports the choice). All compute the
+ * same thing with the same roundings. Calls with more than 1024 distinct
+ * oriented shapes always take the per-phase launches. */
 #define MUON_CARRY_WHEN_C 2
+#define MUON_PERSISTENT_AUTO 2
 typedef struct {
   int32_t steps;
   float a, b, c;
@@ -123,7 +130,7 @@ typedef struct {
 } muon_config;
 
 /* Fills *cfg with the defaults: steps 5, (a,b,c) = (1.5, -0.5, 0), eps 1e-7,
- * scale_lr_by_shape 1, weight_decay 0, precise_carry MUON_CARRY_WHEN_C, persistent 1. The cubic coefficients
+ * scale_lr_by_shape 1, weight_decay 0, precise_carry MUON_CARRY_WHEN_C, persistent MUON_PERSISTENT_AUTO. The cubic coefficients
  * are the iteration's textbook form; the pages give none. */
 void muon_default_config(muon_config* cfg);
 
@@ -221,6 +228,16 @@ muon_status muon_shard_layout(const int64_t* rows, const int64_t* cols, int coun
  * muon_workspace_bytes writes the device memory the plans hold now. */
 muon_status muon_set_workspace_limit(muon_handle h, int64_t bytes);
 muon_status muon_workspace_bytes(muon_handle h, int64_t* bytes);
+
+/* Host-only, no GPU: which launches a handle whose muon_config.persistent is
+ * `persistent` (0, 1 or 2) runs for `count` matrices rows[j] x cols[j] on a
+ * device with `clusters` resident 2-CTA clusters (74 on a B300), c != 0 when
+ * with_c: *use_persistent = 1 for the persistent launch, 0 for the per-phase
+ * launches, and *kblocks_per_cluster the 64-wide k-blocks of one iteration's
+ * 256 x 256 tiles per cluster that MUON_PERSISTENT_AUTO compares with 800.
+ * Either output pointer may be NULL. */
+muon_status muon_launch_choice(const int64_t* rows, const int64_t* cols, int count, int with_c, int clusters,
+                               int persistent, int* use_persistent, double* kblocks_per_cluster);
 
 /* Host-only, no GPU: the work lists of the persistent Newton-Schulz launch
  * (muon_config.persistent) for `count` matrices rows[j] x cols[j], `steps`

@@ -19,6 +19,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "muon.h")
 MUON_OK, MUON_ERR_INVALID, MUON_ERR_CUDA, MUON_ERR_NOMEM, MUON_ERR_UNSUPPORTED, MUON_ERR_TIMEOUT = range(6)
 MUON_F32, MUON_BF16 = 0, 1
 MUON_CARRY_WHEN_C = 2
+MUON_PERSISTENT_AUTO = 2
 KERNEL_KINDS = 9
 
 
@@ -81,6 +82,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "muon_selftest_wait": (c.c_int, [c.c_void_p, c.c_int64, c.c_void_p]),
         "muon_selftest_persistent": (c.c_int, [c.c_void_p, c.c_int64, c.c_void_p]),
         "muon_set_workspace_limit": (c.c_int, [c.c_void_p, c.c_int64]),
+        "muon_launch_choice": (c.c_int, [P(c.c_int64), P(c.c_int64), c.c_int, c.c_int, c.c_int, c.c_int,
+                                         P(c.c_int), P(c.c_double)]),
         "muon_persistent_schedule": (c.c_int, [P(c.c_int64), P(c.c_int64), c.c_int, c.c_int, c.c_int, c.c_int,
                                                P(c.c_int32), c.c_int64, P(c.c_int32), P(c.c_int64)]),
         "muon_shard_layout": (c.c_int, [P(c.c_int64), P(c.c_int64), c.c_int, c.c_int, c.c_int, c.c_int64,
@@ -169,6 +172,22 @@ def plan_stats(shapes: Sequence, with_c: bool = False) -> dict:
     return {"groups": g.value, "gram_tiles": gt.value, "combine_tiles": ct.value, "flops_per_iter": fl.value}
 
 
+def launch_choice(shapes: Sequence, with_c: bool = False, clusters: int = 74, persistent: Optional[bool] = None):
+    """(uses the persistent launch, k-blocks of one iteration per cluster) for a handle whose
+    `persistent` option is given (None: the library default, chosen per call). Host only."""
+    lib = load_library()
+    n = len(shapes)
+    rows = (ctypes.c_int64 * max(1, n))(*[int(r) for r, _ in shapes])
+    cols = (ctypes.c_int64 * max(1, n))(*[int(c) for _, c in shapes])
+    mode = MUON_PERSISTENT_AUTO if persistent is None else int(bool(persistent))
+    use, kb = ctypes.c_int(), ctypes.c_double()
+    st = lib.muon_launch_choice(rows, cols, n, int(bool(with_c)), int(clusters), mode, ctypes.byref(use),
+                                ctypes.byref(kb))
+    if st != MUON_OK:
+        raise MuonError(st, "muon_launch_choice")
+    return bool(use.value), kb.value
+
+
 def persistent_schedule(shapes: Sequence, steps: int, with_c: bool = False, clusters: int = 74):
     """(items, begin) of the persistent launch's work lists (host only): items as an N x 4 list of
     [kind | group << 2 | flags << 12, matrix in group, row | col << 16, counter target]."""
@@ -222,13 +241,15 @@ class Muon:
 
     def __init__(self, device: int = 0, steps: int = 5, a: float = 1.5, b: float = -0.5, c: float = 0.0,
                  eps: float = 1e-7, scale_lr_by_shape: bool = True, weight_decay: float = 0.0,
-                 precise_carry: Optional[bool] = None, persistent: bool = True):
+                 precise_carry: Optional[bool] = None, persistent: Optional[bool] = None):
         self.lib = load_library()
         self.device = device
         # precise_carry: True always, False never, None (the library default) for calls with c != 0
         carry = MUON_CARRY_WHEN_C if precise_carry is None else int(bool(precise_carry))
-        self.config = MuonConfig(steps, a, b, c, eps, int(bool(scale_lr_by_shape)), weight_decay, carry,
-                                 int(bool(persistent)))
+        # persistent: True the persistent launch, False one launch per phase, None (the library default)
+        # chosen per call by the work per cluster
+        mode = MUON_PERSISTENT_AUTO if persistent is None else int(bool(persistent))
+        self.config = MuonConfig(steps, a, b, c, eps, int(bool(scale_lr_by_shape)), weight_decay, carry, mode)
         h = ctypes.c_void_p()
         st = self.lib.muon_create(ctypes.byref(h), device, ctypes.byref(self.config))
         if st != MUON_OK:

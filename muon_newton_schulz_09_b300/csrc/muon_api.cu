@@ -241,7 +241,7 @@ struct muon_ctx {
   // Device memory held by the plans, and the cap on it (0: none; muon_set_workspace_limit).
   size_t plan_bytes = 0;
   size_t plan_limit = 0;
-  bool per_phase = false;  // one launch per Gram / combine phase instead of the persistent launch
+  int launch_mode = MUON_PERSISTENT_AUTO;  // muon_config.persistent
 };
 
 namespace {
@@ -1056,6 +1056,36 @@ muon_status run_iterations(muon_handle h, const Plan& P, int steps, float a, flo
 constexpr int kFusedMaxIters = 16;
 // Shape groups one persistent launch can name (10 bits of a work item); more take the per-phase launches.
 constexpr size_t kFusedMaxGroups = 1024;
+// MUON_PERSISTENT_AUTO takes the per-phase launches once one iteration gives every cluster this many
+// 64-wide k-blocks of 256 x 256 pair tiles or more. Measured in one process (20-step bursts, ms per
+// step, persistent / per-phase): GPT-2 124M step (350 per cluster) 1.027 / 1.054, its quintic (420)
+// 1.520 / 1.593, 64 x 1024^2 (360) 0.911 / 0.960, GPT-2 350M step (1619) 4.725 / 4.695, 4096 x 16384
+// with k = 10 (1356) 7.056 / 6.868: where each phase already streams hundreds of k-blocks per cluster,
+// the per-phase launches' ramps and tails cost less than the persistent launch's item changes.
+constexpr double kAutoPerPhaseKblocks = 800.0;
+
+// 64-wide k-blocks of one Newton-Schulz iteration of every matrix, per cluster: the Gram's upper
+// triangle of 256 x 256 pair tiles (K = m), the A A pass when c != 0 (K = n), the combine (K = n).
+double iteration_kblocks_per_cluster(const std::vector<Group>& groups, bool c_nz, int clusters) {
+  double kb = 0.0;
+  for (const Group& g : groups) {
+    const int64_t nt = ceil_div(g.n, 128), gt2 = ceil_div(g.n, 256), mt = ceil_div(g.m, 256);
+    const int64_t nk_m = ceil_div(g.m, 64), nk_n = ceil_div(g.n, 64);
+    int64_t gram_pairs = 0;
+    for (int64_t J = 0; J < gt2; ++J) gram_pairs += ceil_div(std::min<int64_t>(2 * J + 2, nt), 2);
+    const int64_t comb_pairs = ceil_div(nt, 2) * mt;
+    kb += static_cast<double>(g.count) *
+          static_cast<double>(gram_pairs * nk_m + (c_nz ? gram_pairs * nk_n : 0) + comb_pairs * nk_n);
+  }
+  return kb / std::max(1, clusters);
+}
+
+// Whether a call runs one launch per phase instead of the persistent launch.
+bool per_phase_launches(const std::vector<Group>& groups, int mode, bool c_nz, int clusters) {
+  if (groups.size() > kFusedMaxGroups || mode == 0) return true;
+  if (mode == 1) return false;
+  return iteration_kblocks_per_cluster(groups, c_nz, clusters) >= kAutoPerPhaseKblocks;
+}
 
 struct SimMatrix {
   int slot = 0;
@@ -1372,7 +1402,7 @@ void muon_default_config(muon_config* cfg) {
   cfg->scale_lr_by_shape = 1;
   cfg->weight_decay = 0.0f;
   cfg->precise_carry = MUON_CARRY_WHEN_C;
-  cfg->persistent = 1;
+  cfg->persistent = MUON_PERSISTENT_AUTO;
 }
 
 const char* muon_status_string(muon_status s) {
@@ -1514,6 +1544,23 @@ muon_status muon_plan_stats(const int64_t* rows, const int64_t* cols, int count,
   return MUON_OK;
 }
 
+muon_status muon_launch_choice(const int64_t* rows, const int64_t* cols, int count, int with_c, int clusters,
+                               int persistent, int* use_persistent, double* kblocks_per_cluster) {
+  if (count < 0 || (count > 0 && (!rows || !cols)) || clusters < 1 || persistent < 0 || persistent > 2)
+    return MUON_ERR_INVALID;
+  std::vector<std::pair<int64_t, int64_t>> key(static_cast<size_t>(count));
+  for (int j = 0; j < count; ++j) {
+    if (rows[j] < 0 || cols[j] < 0) return MUON_ERR_INVALID;
+    key[j] = {rows[j], cols[j]};
+  }
+  std::vector<MatInfo> mats;
+  std::vector<Group> grps;
+  group_shapes(key, mats, grps);
+  if (use_persistent) *use_persistent = per_phase_launches(grps, persistent, with_c != 0, clusters) ? 0 : 1;
+  if (kblocks_per_cluster) *kblocks_per_cluster = iteration_kblocks_per_cluster(grps, with_c != 0, clusters);
+  return MUON_OK;
+}
+
 muon_status muon_persistent_schedule(const int64_t* rows, const int64_t* cols, int count, int steps, int with_c,
                                      int clusters, int32_t* items, int64_t items_cap, int32_t* begin,
                                      int64_t* num_items) {
@@ -1550,7 +1597,7 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
   if (cfg && (cfg->steps < 0 || cfg->steps > kMaxSteps || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->a) ||
               !std::isfinite(cfg->b) || !std::isfinite(cfg->c) || !(cfg->weight_decay >= 0.0f) ||
               !std::isfinite(cfg->weight_decay) || (cfg->precise_carry < 0 || cfg->precise_carry > 2) ||
-              (cfg->persistent != 0 && cfg->persistent != 1)))
+              (cfg->persistent < 0 || cfg->persistent > 2)))
     return MUON_ERR_INVALID;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
@@ -1568,7 +1615,7 @@ muon_status muon_create(muon_handle* out, int device, const muon_config* cfg) {
 
   muon_default_config(&h->cfg);
   if (cfg) h->cfg = *cfg;
-  h->per_phase = h->cfg.persistent == 0;
+  h->launch_mode = h->cfg.persistent;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
@@ -1655,7 +1702,7 @@ muon_status muon_orthogonalize(muon_handle h, const muon_matrix* in, const muon_
   if ((st = launch_momentum<false>(h, *P, in, nullptr, 0.f, 0, 0, s)) != MUON_OK) return st;
   if ((st = launch_map<kScale>(h, *P, in, 0, 0.f, s, K_SCALE)) != MUON_OK) return st;
   int xk = 0;
-  if (h->per_phase || P->groups.size() > kFusedMaxGroups) {
+  if (per_phase_launches(P->groups, h->launch_mode, c != 0.0f, h->max_lists)) {
     const bool direct = steps >= 1 && prepare_final(h, *P, out, false, 0.f);
     if ((st = run_iterations(h, *P, steps, a, b, c, s, &xk, direct)) != MUON_OK) return st;
     if (direct) return MUON_OK;
@@ -1687,7 +1734,7 @@ muon_status muon_step(muon_handle h, const muon_matrix* params, const muon_matri
     return st;
   int xk = 0;
   // The update happens in the last combine's epilogue when the parameters allow it.
-  if (h->per_phase || P->groups.size() > kFusedMaxGroups) {
+  if (per_phase_launches(P->groups, h->launch_mode, h->cfg.c != 0.0f, h->max_lists)) {
     const bool direct = steps >= 1 && prepare_final(h, *P, params, true, lr);
     if ((st = run_iterations(h, *P, steps, h->cfg.a, h->cfg.b, h->cfg.c, s, &xk, direct, true)) != MUON_OK)
       return st;

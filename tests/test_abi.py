@@ -28,7 +28,7 @@ def test_default_config():
     cfg = mu.MuonConfig()
     mu.load_library().muon_default_config(ctypes.byref(cfg))
     assert (cfg.steps, cfg.a, cfg.b, cfg.c, cfg.scale_lr_by_shape, cfg.weight_decay, cfg.precise_carry,
-            cfg.persistent) == (5, 1.5, -0.5, 0.0, 1, 0.0, 2, 1)
+            cfg.persistent) == (5, 1.5, -0.5, 0.0, 1, 0.0, 2, 2)
     assert abs(cfg.eps - 1e-7) < 1e-12
 
 

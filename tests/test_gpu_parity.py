@@ -566,6 +566,28 @@ def test_persistent_and_per_phase_launches_agree_bit_for_bit():
             assert np.array_equal(x, y)
 
 
+def test_default_handle_chooses_the_launches_by_work_per_cluster():
+    """The default handle takes the per-phase launches for a 4096 x 16384 matrix (1356 k-blocks per
+    cluster per iteration) and the persistent launch for a small set, as launch_choice says."""
+    from muon_newton_schulz_09_b300 import Muon, launch_choice
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    with Muon(0) as mu:
+        for shapes, persistent in [([(4096, 16384)], False), ([(256, 768), (768, 256)], True)]:
+            assert launch_choice(shapes)[0] is persistent
+            x = [torch.randn(s, device="cuda", generator=gen).to(torch.bfloat16) for s in shapes]
+            out = [torch.empty(s, device="cuda", dtype=torch.bfloat16) for s in shapes]
+            mu.profile_read()
+            mu.profile(True)
+            mu.orthogonalize(x, out, steps=1)
+            torch.cuda.synchronize()
+            mu.profile(False)
+            prof = mu.profile_read()
+            assert mu.get_error() == 0
+            assert prof["newton_schulz"][1] == (1 if persistent else 0)
+            assert prof["gram_xxt"][1] == (0 if persistent else 1)
+            assert prof["combine_ax_bx"][1] == (0 if persistent else 1)
+
+
 def test_quintic_over_several_persistent_launches():
     """20 quintic iterations take two persistent launches (16 + 4): the second starts from the first's
     X, the folded scale applies only in the first and the update only in the last. The default config

@@ -10,7 +10,7 @@ from collections import Counter, defaultdict, deque
 import pytest
 
 import workloads as wl
-from muon_newton_schulz_09_b300 import persistent_schedule
+from muon_newton_schulz_09_b300 import launch_choice, persistent_schedule
 
 GRAM, GRAM_AA, COMB = 0, 1, 2
 FIRST, LAST, ODD = 1, 2, 4
@@ -139,3 +139,45 @@ def test_more_shape_groups_than_an_item_can_name_is_refused():
     with pytest.raises(MuonError) as e:
         persistent_schedule([(1, k) for k in range(1, 1026)], 1, False, 4)
     assert e.value.status == MUON_ERR_UNSUPPORTED
+
+
+def kblocks_per_cluster(shapes, with_c, clusters=74):
+    """One iteration's 64-wide k-blocks of 256 x 256 pair tiles per cluster, rebuilt from the tiles:
+    Gram pairs reaching the upper triangle (K = m), the A A pass (K = n), the combine (K = n)."""
+    kb = 0
+    for n, m, cnt in groups_of(shapes):
+        nt, gt2, mt = -(-n // 128), -(-n // 256), -(-m // 256)
+        gram = sum(len(range(0, min(2 * J + 2, nt), 2)) for J in range(gt2))
+        comb = len(range(0, nt, 2)) * mt
+        kb += cnt * (gram * -(-m // 64) + (gram * -(-n // 64) if with_c else 0) + comb * -(-n // 64))
+    return kb / clusters
+
+
+@pytest.mark.parametrize("name,persistent", [
+    ("gpt2_124m_hidden", True), ("gpt2_124m_hidden_quintic", True), ("square_64x1024", True),
+    ("single_128x256_f32", True), ("gpt2_350m_hidden", False), ("illcond_4096x16384", False)])
+def test_default_launch_choice_by_work_per_cluster(name, persistent):
+    """The default handle runs the persistent launch below 800 k-blocks per cluster per iteration and
+    the per-phase launches from there on: the GPT-2 124M sets (350, 420 with the A A pass) and the
+    1024^2 batch (360) persistent, the GPT-2 350M set (1619) and the 4096 x 16384 matrix (1356) not."""
+    w = wl.WORKLOADS[name]
+    with_c = w.coeffs[2] != 0
+    use, kb = launch_choice(w.shapes, with_c)
+    assert use == persistent
+    assert kb == pytest.approx(kblocks_per_cluster(w.shapes, with_c), rel=1e-12)
+    assert (kb < 800) == persistent
+    # explicit choices are taken as given
+    assert launch_choice(w.shapes, with_c, persistent=True)[0] is True
+    assert launch_choice(w.shapes, with_c, persistent=False)[0] is False
+
+
+def test_launch_choice_thresholds_and_bad_arguments():
+    from muon_newton_schulz_09_b300 import MuonError
+    assert launch_choice(wl.GPT2_124M.shapes)[1] == pytest.approx(25920 / 74)
+    # fewer clusters: more work each, so the same set crosses over
+    assert launch_choice(wl.GPT2_124M.shapes, clusters=32)[0] is False
+    # beyond 1024 shape groups every mode runs the per-phase launches
+    assert launch_choice([(1, k) for k in range(1, 1026)], persistent=True)[0] is False
+    for kw in ({"clusters": 0},):
+        with pytest.raises(MuonError):
+            launch_choice([(64, 64)], **kw)
