@@ -43,8 +43,8 @@ SMS = 148
 # hash gives null.
 NCU_TRAFFIC = {
     # ncu --set full on the GPT-2 124M step: the persistent launch running all 5 iterations
-    # (profiles/persistent_ns_gpt2_124m.md), 2.087 GB read + 1.242 GB written.
-    "dd3861ca46093d56": {"newton_schulz": 3.329e9},
+    # (profiles/persistent_ns_gpt2_124m.md), 2.087 GB read + 1.241 GB written.
+    "bf10e2b8ec7908f5": {"newton_schulz": 3.328e9},
 }
 
 KERNEL_SOURCES = ["muon_newton_schulz_09_b300/csrc/ns_gemm.cuh", "muon_newton_schulz_09_b300/csrc/elementwise.cuh",
