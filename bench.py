@@ -38,14 +38,21 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 DENSE_FLOPS_PER_SM_CYCLE = 8192
 SMS = 148
 
-# DRAM bytes (read + write) per launch of each kernel from one ncu capture, keyed
-# by the hash of the kernel sources' code (comments excluded) they were taken with. A stale
-# hash gives null.
+# DRAM bytes (read + write) per launch of a kernel on a workload, from one ncu capture, keyed by
+# the hash of the kernel sources' code (comments excluded) they were taken with, then by workload
+# and kernel kind. A stale hash, or a workload or kernel without a capture, gives null.
 NCU_TRAFFIC = {
-    # ncu --set full on the GPT-2 124M step: the persistent launch running all 5 iterations
-    # (profiles/persistent_ns_gpt2_124m.md), 2.087 GB read + 1.241 GB written.
-    "bf10e2b8ec7908f5": {"newton_schulz": 3.328e9},
+    "bf10e2b8ec7908f5": {
+        # ncu --set full on the GPT-2 124M step: the persistent launch running all 5 iterations
+        # (profiles/persistent_ns_gpt2_124m.md), 2.087 GB read + 1.241 GB written.
+        "gpt2_124m_hidden": {"newton_schulz": 3.328e9},
+    },
 }
+
+
+def ncu_traffic(workload: str, kernel: str):
+    """The captured DRAM bytes per launch of `kernel` on `workload` at the current sources, or None."""
+    return NCU_TRAFFIC.get(source_hash(), {}).get(workload, {}).get(kernel)
 
 KERNEL_SOURCES = ["muon_newton_schulz_09_b300/csrc/ns_gemm.cuh", "muon_newton_schulz_09_b300/csrc/elementwise.cuh",
                   "muon_newton_schulz_09_b300/csrc/ptx.cuh", "muon_newton_schulz_09_b300/csrc/muon_api.cu",
@@ -537,7 +544,7 @@ def run_ours(args) -> dict:
         kernels[name]["share"] = prof[name][0] / total_ms
     top = max(kernels, key=lambda k: prof[k][0])
     k = kernels[top]
-    traffic = NCU_TRAFFIC.get(source_hash(), {}).get(top)
+    traffic = ncu_traffic(w.name, top)
     roofline = {"kernel": top, "bound": k["bound"], "achieved": round(k["achieved"], 2),
                 "peak": tc_peak if k["bound"] == "tensor" else peaks["hbm_gbs"], "unit": k["unit"],
                 "frac": round(k["frac"], 4), "traffic": traffic,

@@ -114,3 +114,22 @@ def test_peak_choice_follows_the_region_length():
 def test_resident_bytes_of_the_headline_step():
     # bf16 grads (2) + fp32 momentum (4) + bf16 params (2) per element
     assert bench.resident_bytes(wl.GPT2_124M) == 84934656 * 8
+
+
+def test_traffic_is_read_only_for_its_own_workload_and_sources(monkeypatch):
+    """The ncu traffic of one workload's capture is never reported for another workload, another
+    kernel or other kernel sources."""
+    monkeypatch.setattr(bench, "source_hash", lambda: "h1")
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", {"h1": {"gpt2_124m_hidden": {"newton_schulz": 3.0e9}}})
+    assert bench.ncu_traffic("gpt2_124m_hidden", "newton_schulz") == 3.0e9
+    assert bench.ncu_traffic("gpt2_124m_hidden_quintic", "newton_schulz") is None
+    assert bench.ncu_traffic("gpt2_124m_hidden", "momentum_norm") is None
+    monkeypatch.setattr(bench, "source_hash", lambda: "h2")
+    assert bench.ncu_traffic("gpt2_124m_hidden", "newton_schulz") is None
+
+
+def test_traffic_table_entries_name_known_workloads():
+    for per_hash in bench.NCU_TRAFFIC.values():
+        for name, kernels in per_hash.items():
+            assert name in wl.WORKLOADS
+            assert set(kernels) <= set(bench.kernel_work(wl.WORKLOADS[name]))
