@@ -42,10 +42,10 @@ SMS = 148
 # the hash of the kernel sources' code (comments excluded) they were taken with, then by workload
 # and kernel kind. A stale hash, or a workload or kernel without a capture, gives null.
 NCU_TRAFFIC = {
-    "bf10e2b8ec7908f5": {
-        # ncu --set full on the GPT-2 124M step: the persistent launch running all 5 iterations
-        # (profiles/persistent_ns_gpt2_124m.md), 2.087 GB read + 1.241 GB written.
-        "gpt2_124m_hidden": {"newton_schulz": 3.328e9},
+    "1855b12bb7b36373": {
+        # ncu --set full on one per-phase combine of the 4096 x 16384 matrix
+        # (profiles/combine_gemm_illcond_4096x16384.md), 216.0 MB read + 115.5 MB written.
+        "illcond_4096x16384": {"combine_ax_bx": 3.315e8},
     },
 }
 
