@@ -1135,8 +1135,8 @@ void fused_schedule(const Plan& P, bool carry, int iters, bool c_nz, int cluster
         gram_stage(kNsGram, nk_m);
         if (c_nz) gram_stage(kNsGramAA, nk_n);
         std::vector<std::pair<int4, int>> st;
-        for (int I = 0; I < nt; I += kCluster)
-          for (int J = 0; J < mt; ++J)
+        for (int J = 0; J < mt; ++J)  // column by column, as in build_tiles
+          for (int I = 0; I < nt; I += kCluster)
             st.push_back({ns_item(kNsComb, static_cast<int>(gi), flags, b, I, J, halves), nk_n + kFusedTileOverhead});
         halves += 4 * static_cast<int>(st.size());
         M.stages.push_back(std::move(st));
