@@ -42,10 +42,13 @@ SMS = 148
 # the hash of the kernel sources' code (comments excluded) they were taken with, then by workload
 # and kernel kind. A stale hash, or a workload or kernel without a capture, gives null.
 NCU_TRAFFIC = {
-    "1855b12bb7b36373": {
-        # ncu --set full on one per-phase combine of the 4096 x 16384 matrix
-        # (profiles/combine_gemm_illcond_4096x16384.md), 216.0 MB read + 115.5 MB written.
-        "illcond_4096x16384": {"combine_ax_bx": 3.315e8},
+    "c0a396102587b97f": {
+        # ncu --set full on the GPT-2 124M step: the persistent launch running all 5 iterations
+        # (profiles/persistent_ns_gpt2_124m.md), 2.069 GB read + 1.242 GB written.
+        "gpt2_124m_hidden": {"newton_schulz": 3.310e9},
+        # ncu --set full on one per-phase combine and one Gram of the 4096 x 16384 matrix
+        # (profiles/combine_gemm_illcond_4096x16384.md): 218.2 + 115.7 MB and 233.6 + 21.5 MB.
+        "illcond_4096x16384": {"combine_ax_bx": 3.338e8, "gram_xxt": 2.551e8},
     },
 }
 

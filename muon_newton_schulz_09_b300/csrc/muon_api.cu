@@ -1063,9 +1063,9 @@ constexpr int kFusedMaxIters = 16;
 constexpr size_t kFusedMaxGroups = 1024;
 // MUON_PERSISTENT_AUTO takes the per-phase launches once one iteration gives every cluster this many
 // 64-wide k-blocks of 256 x 256 pair tiles or more. Measured in one process (20-step bursts, ms per
-// step, persistent / per-phase): GPT-2 124M step (350 per cluster) 1.027 / 1.054, its quintic (420)
-// 1.520 / 1.593, 64 x 1024^2 (360) 0.911 / 0.960, GPT-2 350M step (1619) 4.725 / 4.695, 4096 x 16384
-// with k = 10 (1356) 7.056 / 6.868: where each phase already streams hundreds of k-blocks per cluster,
+// step, persistent / per-phase): GPT-2 124M step (350 per cluster) 1.023 / 1.052, its quintic (420)
+// 1.508 / 1.588, 64 x 1024^2 (360) 0.904 / 0.956, GPT-2 350M step (1619) 4.665 / 4.652, 4096 x 16384
+// with k = 10 (1356) 6.078 / 5.827: where each phase already streams hundreds of k-blocks per cluster,
 // the per-phase launches' ramps and tails cost less than the persistent launch's item changes.
 constexpr double kAutoPerPhaseKblocks = 800.0;
 
