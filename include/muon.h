@@ -159,6 +159,10 @@ muon_status muon_orthogonalize(muon_handle h, const muon_matrix* in, const muon_
  * params: F32 or BF16 (all alike). grads: F32 or BF16 (all alike).
  * momentum: F32. All three of matrix j have the same rows and cols and must
  * not overlap one another. count == 0 is a no-op. */
+/* Both entry points are stream-ordered. The first call for a set of shapes
+ * allocates and uploads its plan synchronously; later calls with the same
+ * shapes, iteration count and c launch kernels only, so such a call may be
+ * captured in a CUDA graph (the graph keeps the tensors' addresses). */
 muon_status muon_step(muon_handle h, const muon_matrix* params, const muon_matrix* grads,
                       const muon_matrix* momentum, int count, float lr, float beta, int nesterov,
                       void* stream);

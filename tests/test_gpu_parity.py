@@ -588,6 +588,44 @@ def test_default_handle_chooses_the_launches_by_work_per_cluster():
             assert prof["combine_ax_bx"][1] == (0 if persistent else 1)
 
 
+@pytest.mark.parametrize("persistent", [True, False], ids=["persistent", "per_phase"])
+def test_step_replays_from_a_cuda_graph(persistent):
+    """Once a call has built its plan and schedule, a step on fixed tensors issues kernel launches
+    only, so it can be captured in a CUDA graph: each replay is one step, bit for bit what the same
+    step does called directly, with momentum and parameters carried from replay to replay."""
+    from muon_newton_schulz_09_b300 import Muon
+    shapes = [(256, 768), (768, 256), (130, 70), (384, 384)]
+    w, g, m, p = step_case(shapes, "bf16", "bf16", seed=36)
+    lr = 0.02
+    with Muon(0, persistent=persistent) as mu:
+        G = [dev(x, "bf16") for x in g]
+        P, M = [dev(x, "bf16") for x in p], [dev(x, "f32") for x in m]
+        Pe, Me = [t.clone() for t in P], [t.clone() for t in M]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):  # direct calls; the first one builds the plan
+                mu.step(Pe, G, Me, lr=lr, beta=0.95, nesterov=True, stream=s)
+        torch.cuda.synchronize()
+        assert mu.get_error() == 0
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            mu.step(P, G, M, lr=lr, beta=0.95, nesterov=True, stream=s)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert mu.get_error() == 0
+        for a, b in zip(P + M, Pe + Me):
+            assert torch.equal(a, b)
+        # and the replays moved the parameters: three steps of the oracle
+        for j, (r, c) in enumerate(shapes):
+            wj, bj = p[j], m[j]
+            for _ in range(3):
+                wj, bj, o = oracle.muon_step(wj, g[j], bj, lr, 0.95, True, 5, CUBIC)
+            upd = 3 * lr * oracle.lr_scale(r, c) * np.abs(o).max()
+            assert np.all(np.abs(host(P[j]) - wj) <= 3 * bf16_ulp(wj) + 0.05 * upd), (r, c)
+
+
 def test_quintic_over_several_persistent_launches():
     """20 quintic iterations take two persistent launches (16 + 4): the second starts from the first's
     X, the folded scale applies only in the first and the update only in the last. The default config
